@@ -1,0 +1,509 @@
+#!/usr/bin/env python3
+"""Benchmark of one DSA layer-step on GB300: µs per step, HBM GB/s, roofline.
+
+Workload (default): decode, batch 64, every causal length 32768, page 64,
+indexer 64 heads x 128 bf16, top-k 2048, 64 query / 8 KV heads, head dim 128,
+bf16 K/V, softmax scale 1/sqrt(128).  One step = lightning indexer -> top-k
+-> sparse attention (8 splits) -> merge, replayed as one CUDA graph with the
+inputs resident in HBM.  Algorithmic bytes per step: index keys up to each
+length (64 x 32768 x 256 B) + selected K/V (64 x 2048 x 8 heads x 128 x 2 B
+x 2) = 1 GiB.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dsa|reference]
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs an independent
+replica on its own GPU (the step does not shard; no collective on the data
+path) and rank 0 prints the aggregate.  --impl reference times the CPU
+oracle (fp64 numpy, one thread) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+if "--cpu-baseline-worker" in sys.argv or ("--impl" in sys.argv and "reference" in sys.argv):
+    # the oracle is timed on one host thread: pin BLAS before numpy loads
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        os.environ[_v] = "1"
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per DSA layer-step and HBM GB/s (% of roofline), batch 64, 32k ctx, top-k 2048"
+DEFAULT_WORKLOAD = 2
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20  # > 129 MB L2
+CPU_SAMPLE_ROWS = 2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["dsa", "reference"], default="dsa")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--splits", type=int, default=None, help="override the top-k split count")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-worker", default=None, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# workload description and algorithmic bytes
+# ----------------------------------------------------------------------------
+def describe(wl, cfg) -> dict:
+    kd = "fp8 e4m3 + fp32 per-token scale" if wl.idx_key_dtype else "bf16"
+    return {
+        "workload": f"{wl.name}: {wl.kind} step, {wl.max_rows} row slots, indexer {wl.idx_heads}x{wl.idx_dim} {kd}, "
+                    f"page {wl.page_size}, top-k {wl.topk}, {wl.num_q_heads}q/{wl.num_kv_heads}kv heads, "
+                    f"head dim {wl.head_dim} bf16",
+        "batch": int(wl.max_reqs), "score_width": int(wl.score_width), "topk": int(wl.topk),
+        "page_size": int(wl.page_size), "num_splits": int(cfg.num_splits),
+        "l2": "inputs larger than L2 (1 GiB streamed per step) and a 256 MiB L2 flush between steps",
+        "timing": "one CUDA-graph replay per step, CUDA events on the replay stream",
+    }
+
+
+def algorithmic_bytes(wl, rows) -> dict:
+    key_b = wl.idx_dim * (1 if wl.idx_key_dtype else 2) + (4 if wl.idx_key_dtype else 0)
+    idx = 0
+    for b in range(rows["num_blocks"]):
+        f, n = int(rows["block_first"][b]), int(rows["block_nrows"][b])
+        idx += int(max(rows["row_len"][f:f + n])) * key_b
+    kv = sum(min(wl.topk, int(L)) for L in rows["row_len"][:rows["num_rows"]]) * wl.num_kv_heads * wl.head_dim * 2 * 2
+    return {"indexer": idx, "sparse_attn": kv, "step": idx + kv}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    describes the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(kernel)
+    if not rec:
+        return None
+    from sparse_attention_decode_paged_gb300 import build as B
+    src = os.path.join(B.CSRC, rec["source"])
+    import hashlib
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    if h != rec.get("source_sha256"):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.t_on = self.t_off = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["--id=GPU-" + uuid] if uuid else []
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi"] + sel + ["--query-gpu=" + self.FIELDS,
+                                           "--format=csv,noheader,nounits", "-lms", "100"]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, on: bool):
+        if on:
+            self.t_on = time.time()
+        else:
+            self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        rows = []
+        for t, line in self.samples:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((t, float(parts[2]), float(parts[3]), parts[5:]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t_on and self.t_off and self.t_on <= r[0] <= self.t_off + 0.1]
+        window = "timed"
+        if not inside:
+            inside, window = rows, "timed+warmup"
+        if not inside:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[3][1:5]):
+                if v.strip().lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        return {"sm_mhz": float(statistics.median(r[1] for r in inside)),
+                "sm_max_mhz": float(max(r[2] for r in inside)),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle on a bounded sample (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def cpu_sample(inp, nrows: int):
+    """The first `nrows` decode requests of the workload with their pages
+    remapped into a compact pool: a bounded, exact slice of the same step."""
+    import dataclasses
+    wl = inp["workload"]
+    pt = inp["page_table"][:nrows]
+    used = np.unique(pt[pt >= 0])
+    remap = np.full(inp["num_pages"], -1, np.int32)
+    remap[used] = np.arange(used.size, dtype=np.int32)
+    sub_pt = np.where(pt >= 0, remap[np.maximum(pt, 0)], -1).astype(np.int32)
+    sub_wl = dataclasses.replace(wl, max_rows=nrows, max_reqs=nrows)
+    arrays = dict(cache_len=inp["cache_len"][:nrows], new_tokens=inp["new_tokens"][:nrows],
+                  page_table=sub_pt, q_idx=inp["q_idx"][:nrows], w=inp["w"][:nrows],
+                  idx_cache=inp["idx_cache"][used], q=inp["q"][:nrows],
+                  k_cache=inp["k_cache"][used], v_cache=inp["v_cache"][used])
+    if inp["idx_scale"] is not None:
+        arrays["idx_scale"] = inp["idx_scale"][used]
+    return sub_wl, arrays
+
+
+def time_oracle(sub_wl, arrays, reps: int):
+    from oracle import dsa_oracle as O
+    inp = dict(arrays)
+    inp["workload"] = sub_wl
+    inp.setdefault("idx_scale", None)
+    inp["num_pages"] = int(arrays["idx_cache"].shape[0])
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        O.step(inp)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_baseline_worker(path: str):
+    from sparse_attention_decode_paged_gb300 import workloads as W
+    d = np.load(path, allow_pickle=False)
+    meta = json.loads(str(d["meta"]))
+    import dataclasses
+    wl = dataclasses.replace(W.workload(meta["workload"]), max_rows=meta["nrows"], max_reqs=meta["nrows"])
+    arrays = {k: d[k] for k in d.files if k != "meta"}
+    times = time_oracle(wl, arrays, meta["reps"])
+    print(json.dumps({"times": times}))
+
+
+def run_cpu_baseline(inp, wl_index: int, rows_total: int, reps: int = 6):
+    sub_wl, arrays = cpu_sample(inp, CPU_SAMPLE_ROWS)
+    with tempfile.TemporaryDirectory() as td:
+        path = os.path.join(td, "sample.npz")
+        meta = json.dumps({"workload": wl_index, "nrows": CPU_SAMPLE_ROWS, "reps": reps})
+        np.savez(path, meta=np.array(meta), **arrays)
+        env = dict(os.environ)
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[v] = "1"
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker", path],
+                           capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip()[-300:]}
+    times = json.loads(r.stdout.strip().splitlines()[-1])["times"]
+    per_step_s = statistics.median(times) * rows_total / CPU_SAMPLE_ROWS
+    return {"value": per_step_s * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
+            "sample": f"{CPU_SAMPLE_ROWS} of {rows_total} rows (full rows: indexer over all 32768 keys, "
+                      f"top-k, attention), median of {reps} passes, scaled by {rows_total}/{CPU_SAMPLE_ROWS}; "
+                      f"fp64 numpy, one thread"}
+
+
+# ----------------------------------------------------------------------------
+# the reference arm: the CPU oracle, timed on the host
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from sparse_attention_decode_paged_gb300 import workloads as W
+    inp = W.generate(args.workload)
+    wl = inp["workload"]
+    from oracle import dsa_oracle as O
+    rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+    sub_wl, arrays = cpu_sample(inp, CPU_SAMPLE_ROWS)
+    del inp
+    time_oracle(sub_wl, arrays, max(args.warmup, 0))
+    t0 = time.perf_counter()
+    times = time_oracle(sub_wl, arrays, args.steps)
+    wall = time.perf_counter() - t0
+    scale = rows["num_rows"] / CPU_SAMPLE_ROWS
+    us = statistics.mean(times) * scale * 1e6
+    sample = (f"{CPU_SAMPLE_ROWS} of {rows['num_rows']} rows per step (full rows), scaled by "
+              f"{rows['num_rows']}/{CPU_SAMPLE_ROWS}; fp64 numpy, one thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name} (CPU oracle on a bounded sample)", "batch": int(wl.max_reqs),
+                   "score_width": int(wl.score_width), "topk": int(wl.topk)},
+        "cpu_baseline": {"value": us, "unit": "us", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# the CUDA path
+# ----------------------------------------------------------------------------
+def run_dsa(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+
+    from sparse_attention_decode_paged_gb300 import build as B
+    B.build()
+    from sparse_attention_decode_paged_gb300 import dsa
+    from sparse_attention_decode_paged_gb300 import workloads as W
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    t_gen = time.time()
+    inp = W.generate(args.workload)
+    wl = inp["workload"]
+    override = {"num_splits": args.splits} if args.splits else {}
+    dev = DeviceStep(inp, **override)
+    cfg, t, v = dev.cfg, dev.t, dev.views
+    gen_s = time.time() - t_gen
+    nbytes = algorithmic_bytes(wl, dev.rows)
+
+    stream = torch.cuda.Stream()
+    try:
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+        events_in_graph = True
+    except TypeError:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        events_in_graph = False
+
+    def kernels(s, record):
+        if record:
+            ev[0].record(s)
+        dsa.dsa_indexer_scores(cfg, t["q_idx"], t["w"], t["idx_cache"], t["idx_scale"], t["page_table"],
+                               t["row_req"], t["row_len"], t["block_first"], t["block_nrows"],
+                               v["scores"], dev.workspace, s)
+        if record:
+            ev[1].record(s)
+        dsa.dsa_topk(cfg, v["scores"], t["row_len"], v["topk_idx"], dev.workspace, s)
+        if record:
+            ev[2].record(s)
+        dsa.dsa_sparse_attn(cfg, t["q"], t["k_cache"], t["v_cache"], t["page_table"], t["row_req"],
+                            t["row_len"], v["topk_idx"], v["part_m"], v["part_l"], v["part_acc"],
+                            dev.workspace, s)
+        if record:
+            ev[3].record(s)
+        dsa.dsa_merge(cfg, v["part_m"], v["part_l"], v["part_acc"], t["out"], t["lse"], s)
+        if record:
+            ev[4].record(s)
+
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        kernels(stream, record=True)  # eager warm-up (also sets kernel attributes)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        kernels(torch.cuda.current_stream(), record=events_in_graph)
+    torch.cuda.synchronize()
+    status = dsa.dsa_read_device_status(dev.workspace)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for k in range(max(args.warmup, 3)):
+            flush.fill_(k & 0xFF)
+            graph.replay()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        sampler.mark(True)
+        t_wall = time.perf_counter()
+        per_step, per_kernel = [], [[] for _ in range(4)]
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            step_ev[0].record(stream)
+            graph.replay()
+            step_ev[1].record(stream)
+            stream.synchronize()
+            per_step.append(step_ev[0].elapsed_time(step_ev[1]))
+            if events_in_graph:
+                for i in range(4):
+                    per_kernel[i].append(ev[i].elapsed_time(ev[i + 1]))
+        torch.cuda.synchronize()
+        wall_s = time.perf_counter() - t_wall
+        sampler.mark(False)
+        if world > 1:
+            dist.barrier()
+    clocks = sampler.stop()
+
+    if not events_in_graph:  # torch without graph event nodes: time the kernels eagerly instead
+        with torch.cuda.stream(stream):
+            for k in range(max(20, args.steps // 10)):
+                flush.fill_(k & 0xFF)
+                kernels(stream, record=True)
+                stream.synchronize()
+                for i in range(4):
+                    per_kernel[i].append(ev[i].elapsed_time(ev[i + 1]))
+
+    ms_step = statistics.mean(per_step)
+    ms_local = torch.tensor([ms_step], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(ms_local, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_local.item())
+
+    names = ["indexer", "topk", "sparse_attn", "merge"]
+    k_ms = {n: statistics.mean(x) for n, x in zip(names, per_kernel)}
+    dominant = max(("indexer", "sparse_attn"), key=lambda n: k_ms[n])
+    peak, peak_kind = measured_peaks()
+    ach = nbytes[dominant] / (k_ms[dominant] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "traffic": traffic_record(dominant),
+                "algorithmic_bytes": nbytes[dominant], "peak_source": f"{peak_kind} copy bandwidth",
+                "timing": "graph event nodes" if events_in_graph else "eager launches, events"}
+    step_gbs = nbytes["step"] / (ms_max * 1e-3) / 1e9
+    kernel_table = {n: {"us": k_ms[n] * 1e3} for n in names}
+    for n in ("indexer", "sparse_attn"):
+        kernel_table[n]["algorithmic_bytes"] = nbytes[n]
+        kernel_table[n]["gbs"] = nbytes[n] / (k_ms[n] * 1e-3) / 1e9
+        kernel_table[n]["frac_of_peak"] = kernel_table[n]["gbs"] / peak
+
+    # ---- end to end through the public API, host buffers
+    e2e = run_e2e(args, dsa, dev, inp, stream, flush)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            cpu = run_cpu_baseline(inp, args.workload, dev.rows["num_rows"])
+        except Exception as exc:  # report, do not fail the GPU measurement
+            cpu = {"error": repr(exc)[:300]}
+
+    us = ms_max * 1e3 / world  # whole-job µs per layer-step (replicas run concurrently)
+    line = {
+        "metric": METRIC, "value": us, "unit": "us", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": describe(wl, cfg),
+        "rows_per_s": dev.rows["num_rows"] * world / (ms_max * 1e-3),
+        "hbm_gbs_step": step_gbs, "step_roofline_frac": step_gbs / peak,
+        "roofline": roofline, "kernels": kernel_table, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clocks, "gpu_launches": 4 * args.steps, "device_status": status,
+        "median_us": statistics.median(per_step) * 1e3, "min_us": min(per_step) * 1e3,
+        "wall_s": wall_s, "setup_s": gen_s,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, dsa, dev, inp, stream, flush):
+    """µs per step through dsa_build_rows + dsa_step with host buffers: per
+    step, rows are built on the host, the step's inputs are copied from
+    pinned memory, the step runs, and its output is read back."""
+    import torch
+    cfg, t = dev.cfg, dev.t
+    pin = lambda x: x.cpu().pin_memory()  # noqa: E731
+    h_q_idx, h_w, h_q = pin(t["q_idx"]), pin(t["w"]), pin(t["q"])
+    h_pt = pin(t["page_table"])
+    h_rows = {k: torch.empty(cfg.max_rows, dtype=torch.int32).pin_memory()
+              for k in ("row_req", "row_len", "block_first", "block_nrows")}
+    h_out = torch.empty_like(t["out"], device="cpu").pin_memory()
+    h_lse = torch.empty_like(t["lse"], device="cpu").pin_memory()
+    h2d = (h_q_idx.numel() * 2 + h_w.numel() * 4 + h_q.numel() * 2 + h_pt.numel() * 4
+           + 4 * cfg.max_rows * 4)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    cache_len, new_tokens = inp["cache_len"], inp["new_tokens"]
+    times = []
+    with torch.cuda.stream(stream):
+        for k in range(args.e2e_steps + 3):
+            flush.fill_(k & 0xFF)
+            stream.synchronize()
+            t0 = time.perf_counter()
+            rows = dsa.dsa_build_rows(cfg, cache_len, new_tokens)
+            for name, h in h_rows.items():
+                h.numpy()[:] = rows[name]
+                t[name].copy_(h, non_blocking=True)
+            t["page_table"].copy_(h_pt, non_blocking=True)
+            t["q_idx"].copy_(h_q_idx, non_blocking=True)
+            t["w"].copy_(h_w, non_blocking=True)
+            t["q"].copy_(h_q, non_blocking=True)
+            dsa.dsa_step(cfg, dev.args, dev.workspace, stream)
+            h_out.copy_(t["out"], non_blocking=True)
+            h_lse.copy_(t["lse"], non_blocking=True)
+            stream.synchronize()
+            if k >= 3:
+                times.append(time.perf_counter() - t0)
+    return {"value": statistics.median(times) * 1e6, "unit": "us", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": len(times),
+            "path": "dsa_build_rows + pinned H2D + dsa_step (eager) + D2H, wall clock"}
+
+
+def main():
+    args = parse_args()
+    if args.cpu_baseline_worker:
+        cpu_baseline_worker(args.cpu_baseline_worker)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_dsa(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,65 @@
+// Internal interface between the C-ABI layer (dsa_api.cpp) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+struct IndexerParams {
+  const uint8_t *q_idx;     // bf16 [R, H_I, D_I]
+  const float *w;           // [R, H_I]
+  const uint8_t *idx_cache; // bf16 / e4m3 [NP, P, D_I]
+  const float *idx_scale;   // [NP, P] or null
+  const int32_t *page_table;
+  const int32_t *row_req;
+  const int32_t *row_len;
+  const int32_t *block_first;
+  const int32_t *block_nrows;
+  float *scores;            // [R, W]
+  uint32_t *status;
+  int32_t idx_heads, max_rows, max_reqs, max_pages_per_req, score_width, num_pages;
+  int32_t page_size, block_rows;
+};
+
+struct TopkParams {
+  const float *scores;
+  const int32_t *row_len;
+  int32_t *topk_idx;
+  uint32_t *status;
+  int32_t topk, score_width;
+};
+
+struct AttnParams {
+  const uint8_t *q;        // bf16 [R, Hq, D]
+  const uint8_t *k_cache;  // bf16 [NP, P, Hkv, D]
+  const uint8_t *v_cache;
+  const int32_t *page_table;
+  const int32_t *row_req;
+  const int32_t *row_len;
+  const int32_t *topk_idx; // [R, K]
+  float *part_m;           // [R, Hq, S]
+  float *part_l;
+  float *part_acc;         // [R, Hq, S, D]
+  uint32_t *status;
+  int32_t num_q_heads, num_kv_heads, topk, num_splits;
+  int32_t max_reqs, max_pages_per_req, score_width, num_pages, page_size;
+  float sm_scale_log2;     // sm_scale * log2(e)
+};
+
+struct MergeParams {
+  const float *part_m, *part_l, *part_acc;
+  uint8_t *out;  // bf16 [R, Hq, D]
+  float *lse;    // [R, Hq] or null
+  int32_t max_rows, num_q_heads, num_splits;
+};
+
+// Each launcher returns the launch error (cudaSuccess when queued).
+cudaError_t launch_indexer(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st);
+cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, cudaStream_t st);
+cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cudaStream_t st);
+cudaError_t launch_merge(const dsa_config_t &cfg, const MergeParams &p, cudaStream_t st);
+
+}  // namespace dsa

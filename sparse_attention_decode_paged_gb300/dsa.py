@@ -1,0 +1,337 @@
+"""Python binding of libdsa.so (include/dsa.h): argument marshalling only.
+
+Every function has the name of the C entry point it calls and takes torch
+tensors where the C call takes device pointers.  Each checks device,
+dtype, shape and contiguity, passes raw pointers and the current CUDA stream
+(or the one given), and raises DsaError on a non-OK status.  All arithmetic
+of the step runs in the library's CUDA kernels; there is no fallback: if
+libdsa.so cannot be loaded, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsa.so")
+
+DSA_OK = 0
+DSA_ERR_INVALID_ARG = 1
+DSA_ERR_UNSUPPORTED = 2
+DSA_ERR_CAPACITY = 3
+DSA_ERR_CUDA = 4
+DSA_ERR_DEVICE_BOUNDS = 5
+
+DSA_DEV_BAD_ROW = 1 << 0
+DSA_DEV_BAD_PAGE = 1 << 1
+DSA_DEV_BAD_INDEX = 1 << 2
+DSA_DEV_BAD_BLOCK = 1 << 3
+DSA_DEV_TIMEOUT = 1 << 4
+
+DSA_KEY_BF16 = 0
+DSA_KEY_FP8_E4M3 = 1
+
+EXPORTED = (
+    "dsa_validate_config", "dsa_workspace_size", "dsa_workspace_layout",
+    "dsa_reset_device_status", "dsa_read_device_status", "dsa_build_rows",
+    "dsa_indexer_scores", "dsa_topk", "dsa_sparse_attn", "dsa_merge", "dsa_step",
+    "dsa_last_error", "dsa_version",
+)
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"dsa status {status}: {message}")
+        self.status = status
+
+
+class dsa_config_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_q_heads", "num_kv_heads", "head_dim", "idx_heads", "idx_dim", "page_size",
+        "topk", "num_splits", "max_rows", "max_reqs", "max_pages_per_req", "score_width",
+        "num_pages", "block_rows", "idx_key_dtype")] + [("sm_scale", ctypes.c_float)]
+
+
+class dsa_step_args_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "page_table", "row_req", "row_len", "block_first", "block_nrows", "q_idx", "w",
+        "idx_cache", "idx_scale", "q", "k_cache", "v_cache", "out", "lse")]
+
+
+class dsa_workspace_layout_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "status", "scores", "topk_idx", "part_m", "part_l", "part_acc", "total")]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m sparse_attention_decode_paged_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    cfgp = ctypes.POINTER(dsa_config_t)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    proto = {
+        "dsa_validate_config": [cfgp],
+        "dsa_workspace_size": [cfgp, ctypes.POINTER(sz)],
+        "dsa_workspace_layout": [cfgp, ctypes.POINTER(dsa_workspace_layout_t)],
+        "dsa_reset_device_status": [vp, vp],
+        "dsa_read_device_status": [vp, ctypes.POINTER(ctypes.c_uint32), vp],
+        "dsa_build_rows": [cfgp, i32, i32p, i32p, i32p, i32p, i32p, i32p, i32p, i32p, i32p],
+        "dsa_indexer_scores": [cfgp] + [vp] * 12,
+        "dsa_topk": [cfgp] + [vp] * 5,
+        "dsa_sparse_attn": [cfgp] + [vp] * 12,
+        "dsa_merge": [cfgp] + [vp] * 6,
+        "dsa_step": [cfgp, ctypes.POINTER(dsa_step_args_t), vp, vp],
+    }
+    for name, args in proto.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    for name in ("dsa_last_error", "dsa_version"):
+        fn = getattr(lib, name)
+        fn.argtypes = []
+        fn.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int):
+    if status != DSA_OK:
+        raise DsaError(status, _lib.dsa_last_error().decode())
+
+
+def version() -> str:
+    return _lib.dsa_version().decode()
+
+
+# ----------------------------------------------------------------------------
+# config
+# ----------------------------------------------------------------------------
+def make_config(*, num_q_heads, num_kv_heads, head_dim, idx_heads, idx_dim, page_size, topk,
+                num_splits, max_rows, max_reqs, max_pages_per_req, score_width, num_pages,
+                block_rows=1, idx_key_dtype=DSA_KEY_BF16, sm_scale=None) -> dsa_config_t:
+    if sm_scale is None:
+        sm_scale = 1.0 / float(np.sqrt(head_dim))
+    return dsa_config_t(num_q_heads, num_kv_heads, head_dim, idx_heads, idx_dim, page_size, topk,
+                        num_splits, max_rows, max_reqs, max_pages_per_req, score_width,
+                        num_pages, block_rows, idx_key_dtype, float(sm_scale))
+
+
+def config_from_workload(wl, num_pages: int, **override) -> dsa_config_t:
+    kw = dict(num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
+              idx_heads=wl.idx_heads, idx_dim=wl.idx_dim, page_size=wl.page_size,
+              topk=wl.topk, num_splits=wl.num_splits, max_rows=wl.max_rows,
+              max_reqs=wl.max_reqs, max_pages_per_req=wl.max_pages_per_req,
+              score_width=wl.score_width, num_pages=num_pages, block_rows=wl.block_rows,
+              idx_key_dtype=wl.idx_key_dtype, sm_scale=wl.sm_scale)
+    kw.update(override)
+    return make_config(**kw)
+
+
+def dsa_validate_config(cfg: dsa_config_t) -> None:
+    _check(_lib.dsa_validate_config(ctypes.byref(cfg)))
+
+
+def dsa_workspace_size(cfg: dsa_config_t) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.dsa_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return int(n.value)
+
+
+def dsa_workspace_layout(cfg: dsa_config_t) -> dict:
+    lay = dsa_workspace_layout_t()
+    _check(_lib.dsa_workspace_layout(ctypes.byref(cfg), ctypes.byref(lay)))
+    return {name: int(getattr(lay, name)) for name, _ in lay._fields_}
+
+
+# ----------------------------------------------------------------------------
+# pointer marshalling
+# ----------------------------------------------------------------------------
+_BF16 = (torch.bfloat16, torch.int16)
+_FP8 = (torch.float8_e4m3fn, torch.uint8)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t, name, dtypes, numel=None):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements < {numel} required")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ws(workspace):
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise TypeError("workspace: expected a CUDA tensor")
+    return ctypes.c_void_p(workspace.data_ptr())
+
+
+def alloc_workspace(cfg: dsa_config_t, device=None) -> torch.Tensor:
+    """A zeroed uint8 device buffer of dsa_workspace_size(cfg) bytes."""
+    return torch.zeros(dsa_workspace_size(cfg), dtype=torch.uint8, device=device or "cuda")
+
+
+def workspace_views(cfg: dsa_config_t, workspace: torch.Tensor) -> dict:
+    """Typed views of the step intermediates inside a workspace."""
+    lay = dsa_workspace_layout(cfg)
+    R, W, K = cfg.max_rows, cfg.score_width, cfg.topk
+    HS = cfg.num_q_heads * cfg.num_splits
+
+    def view(off, n, dtype, shape):
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        return workspace[off:off + nbytes].view(dtype).view(*shape)
+
+    return dict(
+        status=view(lay["status"], 1, torch.int32, (1,)),
+        scores=view(lay["scores"], R * W, torch.float32, (R, W)),
+        topk_idx=view(lay["topk_idx"], R * K, torch.int32, (R, K)),
+        part_m=view(lay["part_m"], R * HS, torch.float32, (R, cfg.num_q_heads, cfg.num_splits)),
+        part_l=view(lay["part_l"], R * HS, torch.float32, (R, cfg.num_q_heads, cfg.num_splits)),
+        part_acc=view(lay["part_acc"], R * HS * cfg.head_dim, torch.float32,
+                      (R, cfg.num_q_heads, cfg.num_splits, cfg.head_dim)),
+    )
+
+
+# ----------------------------------------------------------------------------
+# entry points
+# ----------------------------------------------------------------------------
+def dsa_reset_device_status(workspace, stream=None) -> None:
+    _check(_lib.dsa_reset_device_status(_ws(workspace), _stream(stream)))
+
+
+def dsa_read_device_status(workspace, stream=None) -> int:
+    """The sticky device status word (synchronizes the stream)."""
+    v = ctypes.c_uint32(0)
+    st = _lib.dsa_read_device_status(_ws(workspace), ctypes.byref(v), _stream(stream))
+    if st not in (DSA_OK, DSA_ERR_DEVICE_BOUNDS):
+        _check(st)
+    return int(v.value)
+
+
+def dsa_build_rows(cfg: dsa_config_t, req_cache_len, req_new_tokens) -> dict:
+    """Host row builder.  Inputs: int sequences; outputs: numpy int32 arrays."""
+    cl = np.ascontiguousarray(np.asarray(req_cache_len, dtype=np.int32))
+    nt = np.ascontiguousarray(np.asarray(req_new_tokens, dtype=np.int32))
+    if cl.shape != nt.shape or cl.ndim != 1:
+        raise ValueError("req_cache_len and req_new_tokens must be 1-D and equal in length")
+    R = cfg.max_rows
+    outs = {k: np.zeros(R, np.int32) for k in ("row_req", "row_len", "row_pos", "block_first", "block_nrows")}
+    nr, nb = ctypes.c_int32(0), ctypes.c_int32(0)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+
+    def ptr(a):
+        return a.ctypes.data_as(i32p)
+
+    _check(_lib.dsa_build_rows(ctypes.byref(cfg), int(cl.size), ptr(cl), ptr(nt),
+                               ptr(outs["row_req"]), ptr(outs["row_len"]), ptr(outs["row_pos"]),
+                               ptr(outs["block_first"]), ptr(outs["block_nrows"]),
+                               ctypes.byref(nr), ctypes.byref(nb)))
+    outs["num_rows"] = int(nr.value)
+    outs["num_blocks"] = int(nb.value)
+    return outs
+
+
+def dsa_indexer_scores(cfg, q_idx, w, idx_cache, idx_scale, page_table, row_req, row_len,
+                       block_first, block_nrows, scores, workspace, stream=None) -> None:
+    R = cfg.max_rows
+    keyt = _FP8 if cfg.idx_key_dtype == DSA_KEY_FP8_E4M3 else _BF16
+    _check(_lib.dsa_indexer_scores(
+        ctypes.byref(cfg),
+        _dev(q_idx, "q_idx", _BF16, R * cfg.idx_heads * cfg.idx_dim),
+        _dev(w, "w", (torch.float32,), R * cfg.idx_heads),
+        _dev(idx_cache, "idx_cache", keyt, cfg.num_pages * cfg.page_size * cfg.idx_dim),
+        _dev(idx_scale, "idx_scale", (torch.float32,), cfg.num_pages * cfg.page_size),
+        _dev(page_table, "page_table", (torch.int32,), cfg.max_reqs * cfg.max_pages_per_req),
+        _dev(row_req, "row_req", (torch.int32,), R), _dev(row_len, "row_len", (torch.int32,), R),
+        _dev(block_first, "block_first", (torch.int32,), R),
+        _dev(block_nrows, "block_nrows", (torch.int32,), R),
+        _dev(scores, "scores", (torch.float32,), R * cfg.score_width),
+        _ws(workspace), _stream(stream)))
+
+
+def dsa_topk(cfg, scores, row_len, topk_idx, workspace, stream=None) -> None:
+    R = cfg.max_rows
+    _check(_lib.dsa_topk(
+        ctypes.byref(cfg), _dev(scores, "scores", (torch.float32,), R * cfg.score_width),
+        _dev(row_len, "row_len", (torch.int32,), R),
+        _dev(topk_idx, "topk_idx", (torch.int32,), R * cfg.topk), _ws(workspace), _stream(stream)))
+
+
+def dsa_sparse_attn(cfg, q, k_cache, v_cache, page_table, row_req, row_len, topk_idx, part_m,
+                    part_l, part_acc, workspace, stream=None) -> None:
+    R, Hq, S, D = cfg.max_rows, cfg.num_q_heads, cfg.num_splits, cfg.head_dim
+    kv = cfg.num_pages * cfg.page_size * cfg.num_kv_heads * D
+    _check(_lib.dsa_sparse_attn(
+        ctypes.byref(cfg), _dev(q, "q", _BF16, R * Hq * D), _dev(k_cache, "k_cache", _BF16, kv),
+        _dev(v_cache, "v_cache", _BF16, kv),
+        _dev(page_table, "page_table", (torch.int32,), cfg.max_reqs * cfg.max_pages_per_req),
+        _dev(row_req, "row_req", (torch.int32,), R), _dev(row_len, "row_len", (torch.int32,), R),
+        _dev(topk_idx, "topk_idx", (torch.int32,), R * cfg.topk),
+        _dev(part_m, "part_m", (torch.float32,), R * Hq * S),
+        _dev(part_l, "part_l", (torch.float32,), R * Hq * S),
+        _dev(part_acc, "part_acc", (torch.float32,), R * Hq * S * D),
+        _ws(workspace), _stream(stream)))
+
+
+def dsa_merge(cfg, part_m, part_l, part_acc, out, lse=None, stream=None) -> None:
+    R, Hq, S, D = cfg.max_rows, cfg.num_q_heads, cfg.num_splits, cfg.head_dim
+    _check(_lib.dsa_merge(
+        ctypes.byref(cfg), _dev(part_m, "part_m", (torch.float32,), R * Hq * S),
+        _dev(part_l, "part_l", (torch.float32,), R * Hq * S),
+        _dev(part_acc, "part_acc", (torch.float32,), R * Hq * S * D),
+        _dev(out, "out", _BF16, R * Hq * D), _dev(lse, "lse", (torch.float32,), R * Hq),
+        _stream(stream)))
+
+
+STEP_FIELDS = ("page_table", "row_req", "row_len", "block_first", "block_nrows", "q_idx", "w",
+               "idx_cache", "idx_scale", "q", "k_cache", "v_cache", "out", "lse")
+
+
+def make_step_args(cfg, t: dict) -> dsa_step_args_t:
+    """Pack a dict of device tensors (keys = STEP_FIELDS) into dsa_step_args_t."""
+    R, Hq, D = cfg.max_rows, cfg.num_q_heads, cfg.head_dim
+    keyt = _FP8 if cfg.idx_key_dtype == DSA_KEY_FP8_E4M3 else _BF16
+    kv = cfg.num_pages * cfg.page_size * cfg.num_kv_heads * D
+    i32 = (torch.int32,)
+    f32 = (torch.float32,)
+    spec = dict(page_table=(i32, cfg.max_reqs * cfg.max_pages_per_req), row_req=(i32, R),
+                row_len=(i32, R), block_first=(i32, R), block_nrows=(i32, R),
+                q_idx=(_BF16, R * cfg.idx_heads * cfg.idx_dim), w=(f32, R * cfg.idx_heads),
+                idx_cache=(keyt, cfg.num_pages * cfg.page_size * cfg.idx_dim),
+                idx_scale=(f32, cfg.num_pages * cfg.page_size), q=(_BF16, R * Hq * D),
+                k_cache=(_BF16, kv), v_cache=(_BF16, kv), out=(_BF16, R * Hq * D),
+                lse=(f32, R * Hq))
+    a = dsa_step_args_t()
+    for name in STEP_FIELDS:
+        dt, n = spec[name]
+        p = _dev(t.get(name), name, dt, n)
+        setattr(a, name, p.value if p is not None else None)
+    return a
+
+
+def dsa_step(cfg, args, workspace, stream=None) -> None:
+    """args: a dsa_step_args_t (see make_step_args) or a dict of tensors."""
+    if isinstance(args, dict):
+        args = make_step_args(cfg, args)
+    _check(_lib.dsa_step(ctypes.byref(cfg), ctypes.byref(args), _ws(workspace), _stream(stream)))

@@ -1,0 +1,83 @@
+"""Device-side plumbing around the C-ABI: upload one step's inputs, build the
+rows through the library, hold the outputs and workspace, run or capture a
+step.  PyTorch is used here only for device memory, streams and CUDA graphs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import dsa
+
+
+def to_device(a: np.ndarray | None, device="cuda", kind: str = "raw"):
+    """numpy -> CUDA tensor; kind 'bf16' reinterprets uint16 bits as bfloat16."""
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if kind == "bf16":
+        t = torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(a).to(device)
+    return t
+
+
+class DeviceStep:
+    """All device buffers of one DSA layer-step for a generated workload."""
+
+    def __init__(self, inp: dict, device="cuda", **cfg_override):
+        wl = inp["workload"]
+        self.inp = inp
+        self.cfg = dsa.config_from_workload(wl, inp["num_pages"], **cfg_override)
+        dsa.dsa_validate_config(self.cfg)
+        self.rows = dsa.dsa_build_rows(self.cfg, inp["cache_len"], inp["new_tokens"])
+        R, Hq, D = wl.max_rows, wl.num_q_heads, wl.head_dim
+        t = {}
+        t["page_table"] = to_device(inp["page_table"], device)
+        for k in ("row_req", "row_len", "block_first", "block_nrows"):
+            t[k] = to_device(self.rows[k], device)
+        t["q_idx"] = to_device(inp["q_idx"], device, "bf16")
+        t["w"] = to_device(inp["w"], device)
+        if inp["idx_scale"] is None:
+            t["idx_cache"] = to_device(inp["idx_cache"], device, "bf16")
+            t["idx_scale"] = None
+        else:
+            t["idx_cache"] = to_device(inp["idx_cache"], device)
+            t["idx_scale"] = to_device(inp["idx_scale"], device)
+        t["q"] = to_device(inp["q"], device, "bf16")
+        t["k_cache"] = to_device(inp["k_cache"], device, "bf16")
+        t["v_cache"] = to_device(inp["v_cache"], device, "bf16")
+        t["out"] = torch.zeros(R, Hq, D, dtype=torch.bfloat16, device=device)
+        t["lse"] = torch.zeros(R, Hq, dtype=torch.float32, device=device)
+        self.t = t
+        self.workspace = dsa.alloc_workspace(self.cfg, device)
+        self.views = dsa.workspace_views(self.cfg, self.workspace)
+        self.args = dsa.make_step_args(self.cfg, t)
+
+    def step(self, stream=None):
+        dsa.dsa_step(self.cfg, self.args, self.workspace, stream)
+
+    def status(self) -> int:
+        return dsa.dsa_read_device_status(self.workspace)
+
+    def capture(self, stream: torch.cuda.Stream | None = None) -> torch.cuda.CUDAGraph:
+        """Warm up once eagerly, then capture one step into a CUDA graph."""
+        stream = stream or torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            self.step(stream)
+        torch.cuda.current_stream().wait_stream(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.step(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return g
+
+    def set_rows(self, cache_len, new_tokens, page_table=None):
+        """Rebuild rows on the host and copy them into the static buffers."""
+        self.rows = dsa.dsa_build_rows(self.cfg, cache_len, new_tokens)
+        for k in ("row_req", "row_len", "block_first", "block_nrows"):
+            self.t[k].copy_(torch.from_numpy(self.rows[k]))
+        if page_table is not None:
+            self.t["page_table"].copy_(torch.from_numpy(np.ascontiguousarray(page_table)))

@@ -15,3 +15,23 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def dsa_lib():
+    """Builds libdsa.so if needed (nvcc cross-compiles here) and imports the binding."""
+    from sparse_attention_decode_paged_gb300 import build
+
+    build.build()
+    from sparse_attention_decode_paged_gb300 import dsa
+
+    return dsa
+
+
+@pytest.fixture(scope="session")
+def cuda_ok():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return True

@@ -1,0 +1,265 @@
+"""Edge cases of the CUDA path: exact integer cases, top-k ties and
+infinities, CUDA-graph replay with changed metadata, device-side bounds
+flags, poisoned cache slots and page relabelling."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dsa_oracle as O
+from sparse_attention_decode_paged_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev_step(inp, **kw):
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    dev = DeviceStep(inp, **kw)
+    dev.step()
+    torch.cuda.synchronize()
+    return dev
+
+
+def _bf16_bits_of(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# indexer: integer-valued inputs make every fp32 sum exact
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("fp8", [False, True])
+def test_indexer_exact_on_integer_inputs(fp8, dsa_lib, cuda_ok):
+    wl = W.workload(1)
+    if fp8:
+        wl = dataclasses.replace(wl, idx_key_dtype=W.KEY_FP8_E4M3)
+    inp = W.generate(wl)
+    rng = np.random.default_rng(21)
+    R, HI, DI = wl.max_rows, wl.idx_heads, wl.idx_dim
+    inp["q_idx"] = _bf16_bits_of(rng.integers(-3, 4, (R, HI, DI)))
+    inp["w"] = (2.0 ** rng.integers(-2, 2, (R, HI)) * rng.choice([-1.0, 1.0], (R, HI))).astype(np.float32)
+    keys = rng.integers(-4, 5, inp["idx_cache"].shape).astype(np.float32)
+    if fp8:
+        inp["idx_cache"] = torch.from_numpy(keys).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        inp["idx_scale"] = (2.0 ** rng.integers(-3, 3, inp["idx_scale"].shape)).astype(np.float32)
+    else:
+        inp["idx_cache"] = _bf16_bits_of(keys)
+    dev = _dev_step(inp)
+    rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+    want = O.indexer_scores(inp, rows)
+    got = dev.views["scores"].cpu().numpy().astype(np.float64)
+    for r in range(rows["num_rows"]):
+        L = rows["row_len"][r]
+        assert np.array_equal(got[r, :L], want[r, :L]), r
+    assert dev.status() == 0
+
+
+# ----------------------------------------------------------------------------
+# top-k: crafted rows
+# ----------------------------------------------------------------------------
+def _topk_cfg(dsa_lib, R, W_, K):
+    return dsa_lib.make_config(num_q_heads=8, num_kv_heads=1, head_dim=64, idx_heads=8, idx_dim=32,
+                               page_size=64, topk=K, num_splits=1, max_rows=R, max_reqs=R,
+                               max_pages_per_req=(W_ + 63) // 64, score_width=W_, num_pages=1)
+
+
+@pytest.mark.parametrize("W_,K", [(4096, 512), (32768, 2048), (131072, 2048), (300, 16)])
+def test_topk_crafted_rows(W_, K, dsa_lib, cuda_ok):
+    rng = np.random.default_rng(W_ + K)
+    R = 12
+    cfg = _topk_cfg(dsa_lib, R, W_, K)
+    lens = [0, 1, K - 1, K, K + 1, W_, W_, W_, W_, int(rng.integers(K, W_ + 1)), W_ - 1, W_]
+    s = rng.standard_normal((R, W_)).astype(np.float32)
+    s[5] = 1.0                                                   # all equal: lowest positions win
+    s[6] = rng.choice(np.array([-np.inf, -1.0, 0.0, 2.0, np.nan], np.float32), W_)  # heavy ties + inf + nan
+    s[7] = -np.inf
+    s[7, rng.integers(0, W_, K // 3)] = 3.0                      # few finite, rest -inf
+    s[8] = np.nan
+    s[8, rng.integers(0, W_, K // 2)] = -np.inf                  # -inf beats NaN
+    s[10] = np.round(rng.standard_normal(W_) * 4) / 4            # quantised ties
+    s[10][::7] = -0.0                                            # -0 ties with +0
+    s[11] = np.float32(0.0)
+    s[11, ::3] = -0.0
+    scores = torch.from_numpy(s).cuda()
+    row_len = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = torch.full((R, K), -7, dtype=torch.int32, device="cuda")
+    ws = dsa_lib.alloc_workspace(cfg)
+    dsa_lib.dsa_topk(cfg, scores, row_len, out, ws)
+    got = out.cpu().numpy()
+    for r in range(R):
+        want = O.topk_row(s[r], lens[r], K) if lens[r] else np.full(K, -1, np.int32)
+        assert np.array_equal(got[r], want), (r, lens[r])
+    assert dsa_lib.dsa_read_device_status(ws) == 0
+
+
+def test_topk_random_ragged(dsa_lib, cuda_ok):
+    rng = np.random.default_rng(99)
+    R, W_, K = 64, 8192, 700
+    cfg = _topk_cfg(dsa_lib, R, W_, K)
+    for trial in range(3):
+        lens = rng.integers(0, W_ + 1, R)
+        pool = rng.standard_normal(int(rng.integers(2, 5000))).astype(np.float32)
+        s = pool[rng.integers(0, pool.size, (R, W_))]
+        scores = torch.from_numpy(s).cuda()
+        out = torch.empty((R, K), dtype=torch.int32, device="cuda")
+        ws = dsa_lib.alloc_workspace(cfg)
+        dsa_lib.dsa_topk(cfg, scores, torch.from_numpy(lens.astype(np.int32)).cuda(), out, ws)
+        got = out.cpu().numpy()
+        for r in range(R):
+            want = O.topk_row(s[r], int(lens[r]), K) if lens[r] else np.full(K, -1, np.int32)
+            assert np.array_equal(got[r], want), (trial, r)
+
+
+# ----------------------------------------------------------------------------
+# CUDA graphs: capture once, replay with new device metadata
+# ----------------------------------------------------------------------------
+def test_graph_replay_follows_metadata(dsa_lib, cuda_ok):
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    inp = W.generate(1)
+    wl = inp["workload"]
+    dev = DeviceStep(inp)
+    graph = dev.capture()
+    graph.replay()
+    torch.cuda.synchronize()
+    out_g1 = dev.t["out"].clone()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g1.view(torch.int16), dev.t["out"].view(torch.int16))  # deterministic
+    dev.step()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g1.view(torch.int16), dev.t["out"].view(torch.int16))  # graph == eager
+
+    # new lengths (within each request's pages), fewer live requests, and a
+    # relabelled page table: same buffers, no re-capture
+    rng = np.random.default_rng(3)
+    cl = inp["cache_len"].copy()
+    new_cl = np.array([int(rng.integers(1, c + 1)) for c in cl], np.int32)
+    new_cl[0] = 1
+    new_cl[1] = wl.topk + 1
+    nt = np.ones_like(new_cl)
+    nt[5:] = 0  # requests 5..7 idle this step
+    perm = rng.permutation(inp["num_pages"]).astype(np.int32)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size)
+    pt = inp["page_table"].copy()
+    pt[pt >= 0] = perm[pt[pt >= 0]]
+    for key in ("idx_cache", "k_cache", "v_cache"):
+        src = inp[key][inv]
+        dst = dev.t[key]
+        dst.view(torch.int16 if dst.dtype == torch.bfloat16 else dst.dtype).copy_(
+            torch.from_numpy(src.view(np.int16) if src.dtype == np.uint16 else src))
+    dev.set_rows(new_cl, nt, pt)
+    graph.replay()
+    torch.cuda.synchronize()
+    out_g2 = dev.t["out"].clone()
+    idx_g2 = dev.views["topk_idx"].clone()
+    dev.step()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g2.view(torch.int16), dev.t["out"].view(torch.int16))
+    assert dev.status() == 0
+
+    inp2 = dict(inp)
+    inp2["cache_len"], inp2["new_tokens"] = new_cl, nt
+    inp2["page_table"] = pt
+    for key in ("idx_cache", "k_cache", "v_cache"):
+        inp2[key] = inp[key][inv]
+    rows = O.build_rows(new_cl, nt, wl.max_rows, wl.block_rows)
+    assert rows["num_rows"] == 5
+    q = O.bf16_bits_to_f64(inp2["q"])
+    got_out = out_g2.float().cpu().numpy()
+    idx = idx_g2.cpu().numpy()
+    scores = dev.views["scores"].cpu().numpy()
+    for r in range(wl.max_rows):
+        L = int(rows["row_len"][r])
+        if L == 0:
+            assert (idx[r] == -1).all() and (got_out[r] == 0).all()
+            continue
+        assert np.array_equal(idx[r], O.topk_row(scores[r], L, wl.topk))
+        sel = idx[r][idx[r] >= 0]
+        k, v = O.kv_rows(inp2, int(rows["row_req"][r]), sel)
+        o, _ = O.attention_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads)
+        np.testing.assert_allclose(got_out[r], o, atol=1e-2, rtol=2e-2)
+
+
+# ----------------------------------------------------------------------------
+# invariances on the GPU
+# ----------------------------------------------------------------------------
+def test_poisoned_slots_past_length_change_nothing(dsa_lib, cuda_ok):
+    inp = W.generate(0)
+    wl = inp["workload"]
+    ref = _dev_step(inp)
+    bad = dict(inp)
+    for key in ("idx_cache", "k_cache", "v_cache"):
+        bad[key] = inp[key].copy()
+    for b, L in enumerate(inp["cache_len"]):
+        page = inp["page_table"][b, (L - 1) // wl.page_size]
+        if L % wl.page_size:
+            bad["idx_cache"][page, L % wl.page_size:] = 0x7FC0
+            bad["k_cache"][page, L % wl.page_size:] = 0x7F80
+            bad["v_cache"][page, L % wl.page_size:] = 0x7FC0
+    got = _dev_step(bad)
+    assert torch.equal(ref.views["topk_idx"], got.views["topk_idx"])
+    assert torch.equal(ref.t["out"].view(torch.int16), got.t["out"].view(torch.int16))
+
+
+def test_page_relabelling_is_bit_identical(dsa_lib, cuda_ok):
+    inp = W.generate(1)
+    ref = _dev_step(inp)
+    rng = np.random.default_rng(8)
+    perm = rng.permutation(inp["num_pages"]).astype(np.int32)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size)
+    moved = dict(inp)
+    for key in ("idx_cache", "k_cache", "v_cache"):
+        moved[key] = inp[key][inv]
+    pt = inp["page_table"].copy()
+    pt[pt >= 0] = perm[pt[pt >= 0]]
+    moved["page_table"] = pt
+    got = _dev_step(moved)
+    assert torch.equal(ref.views["scores"], got.views["scores"])
+    assert torch.equal(ref.t["out"].view(torch.int16), got.t["out"].view(torch.int16))
+
+
+# ----------------------------------------------------------------------------
+# device-side bounds checks: flagged, skipped, never a fault
+# ----------------------------------------------------------------------------
+def test_device_bounds_flags(dsa_lib, cuda_ok):
+    inp = W.generate(0)
+    dev = _dev_step(inp)
+    assert dev.status() == 0
+    t, cfg = dev.t, dev.cfg
+
+    # a page id outside the pool, inside request 1's length
+    saved = t["page_table"].clone()
+    t["page_table"][1, 2] = cfg.num_pages + 3
+    dev.step()
+    st = dev.status()
+    assert st & dsa_lib.DSA_DEV_BAD_PAGE
+    t["page_table"].copy_(saved)
+    dsa_lib.dsa_reset_device_status(dev.workspace)
+
+    # a row longer than the score width
+    saved_len = t["row_len"].clone()
+    t["row_len"][0] = cfg.score_width + 1
+    dev.step()
+    st = dev.status()
+    assert st & dsa_lib.DSA_DEV_BAD_BLOCK and st & dsa_lib.DSA_DEV_BAD_ROW
+    assert (dev.views["topk_idx"][0] == -1).all()
+    t["row_len"].copy_(saved_len)
+    dsa_lib.dsa_reset_device_status(dev.workspace)
+
+    # a selected position at or past the row's length
+    idx = dev.views["topk_idx"].clone()
+    dev.step()
+    idx = dev.views["topk_idx"].clone()
+    idx[0, 0] = int(dev.rows["row_len"][0]) + 5
+    idx[1, 1] = -9
+    v = dev.views
+    dsa_lib.dsa_sparse_attn(cfg, t["q"], t["k_cache"], t["v_cache"], t["page_table"], t["row_req"],
+                            t["row_len"], idx, v["part_m"], v["part_l"], v["part_acc"], dev.workspace)
+    assert dev.status() & dsa_lib.DSA_DEV_BAD_INDEX
+    dsa_lib.dsa_reset_device_status(dev.workspace)
+    dev.step()
+    assert dev.status() == 0

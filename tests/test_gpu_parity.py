@@ -1,0 +1,195 @@
+"""CUDA path (through the C-ABI) against the fp64 CPU oracle.
+
+Tolerances (written here, applied element by element):
+  indexer scores : |g - o| <= rtol*|o| + rtol*rms(o over the row),
+                   rtol 2e-2 for bf16 keys, 6e-2 for fp8 keys;
+  top-k indices  : bit-exact, given the GPU's own scores as input to both;
+  attention      : |g - o| <= 1e-2 + 2e-2*|o| on the GPU's selected set
+                   (output and lse), partials likewise.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import dsa_oracle as O
+from sparse_attention_decode_paged_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+RTOL_SCORE = {W.KEY_BF16: 2e-2, W.KEY_FP8_E4M3: 6e-2}
+ATOL_OUT, RTOL_OUT = 1e-2, 2e-2
+
+# rows the oracle recomputes one by one (all rows where that takes seconds)
+SAMPLE_ROWS = {
+    0: None, 1: None, 2: None, 4: None,
+    3: [0, 1, 17, 30, 46, 47, 48, 49, 50, 51, 52, 100, 203, 300, 301, 302, 303, 450, 558, 559, 560, 1023],
+}
+
+
+@pytest.fixture(scope="module", params=range(5), ids=lambda i: f"workload{i}")
+def problem(request, dsa_lib, cuda_ok):
+    """Generated inputs + device buffers of one workload, after one step.
+
+    Module-scoped and parametrized, so pytest runs every test of a workload
+    before generating the next one."""
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    i = request.param
+    inp = W.generate(i)
+    dev = DeviceStep(inp)
+    dev.step()
+    torch.cuda.synchronize()
+    yield i, inp, dev
+    del dev
+    torch.cuda.empty_cache()
+
+
+def _rows(inp):
+    wl = inp["workload"]
+    return O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+
+
+def _sample(i, rows):
+    s = SAMPLE_ROWS[i]
+    if s is None:
+        return list(range(rows["num_rows"]))
+    return [r for r in s if r < len(rows["row_len"])]
+
+
+def _score_ok(g, o, rtol):
+    o = np.asarray(o, np.float64)
+    rms = np.sqrt(np.mean(o * o)) if o.size else 0.0
+    err = np.abs(np.asarray(g, np.float64) - o)
+    bound = rtol * np.abs(o) + rtol * rms
+    return bool(np.all(err <= bound)), float(np.max(err / np.maximum(bound, 1e-30))) if o.size else 0.0
+
+
+def _bf16_to_f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+def test_step_status_clean(problem):
+    i, inp, dev = problem
+    assert dev.status() == 0
+    assert dev.rows["num_rows"] == _rows(inp)["num_rows"]
+
+
+def test_indexer_scores_vs_oracle(problem):
+    i, inp, dev = problem
+    wl = inp["workload"]
+    rows = _rows(inp)
+    scores = dev.views["scores"].cpu().numpy()
+    qi = O.bf16_bits_to_f64(inp["q_idx"])
+    worst = 0.0
+    for r in _sample(i, rows):
+        L = int(rows["row_len"][r])
+        if L == 0:
+            continue
+        keys, sc = O.index_keys(inp, int(rows["row_req"][r]), L)
+        want = O.indexer_scores_row(qi[r], inp["w"][r], keys, sc)
+        ok, ratio = _score_ok(scores[r, :L], want, RTOL_SCORE[wl.idx_key_dtype])
+        worst = max(worst, ratio)
+        assert ok, (r, ratio)
+    print(f"workload {i}: worst score error / tolerance = {worst:.3e}")
+
+
+def test_indexer_writes_nothing_past_length(problem, dsa_lib):
+    i, inp, dev = problem
+    cfg = dev.cfg
+    sentinel = torch.full((cfg.max_rows, cfg.score_width), 12345.0, device="cuda")
+    t = dev.t
+    dsa_lib.dsa_indexer_scores(cfg, t["q_idx"], t["w"], t["idx_cache"], t["idx_scale"], t["page_table"],
+                               t["row_req"], t["row_len"], t["block_first"], t["block_nrows"],
+                               sentinel, dev.workspace)
+    s = sentinel.cpu().numpy()
+    L = dev.rows["row_len"]
+    for r in range(cfg.max_rows):
+        assert (s[r, L[r]:] == 12345.0).all(), r
+        if L[r]:
+            assert np.array_equal(s[r, :L[r]], dev.views["scores"][r, :L[r]].cpu().numpy())
+    assert dev.status() == 0
+
+
+def test_topk_bit_exact_on_gpu_scores(problem):
+    i, inp, dev = problem
+    wl = inp["workload"]
+    rows = _rows(inp)
+    scores = dev.views["scores"].cpu().numpy()
+    got = dev.views["topk_idx"].cpu().numpy()
+    for r in range(wl.max_rows):
+        L = int(rows["row_len"][r])
+        want = O.topk_row(scores[r], L, wl.topk) if L else np.full(wl.topk, -1, np.int32)
+        assert np.array_equal(got[r], want), r
+
+
+def test_attention_vs_oracle_on_gpu_selection(problem):
+    i, inp, dev = problem
+    wl = inp["workload"]
+    rows = _rows(inp)
+    idx = dev.views["topk_idx"].cpu().numpy()
+    out = _bf16_to_f64(dev.t["out"])
+    lse = dev.t["lse"].cpu().numpy().astype(np.float64)
+    q = O.bf16_bits_to_f64(inp["q"])
+    for r in _sample(i, rows):
+        L = int(rows["row_len"][r])
+        if L == 0:
+            continue
+        sel = idx[r][idx[r] >= 0]
+        k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel)
+        o, ls = O.attention_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads)
+        np.testing.assert_allclose(out[r], o, atol=ATOL_OUT, rtol=RTOL_OUT, err_msg=f"row {r}")
+        np.testing.assert_allclose(lse[r], ls, atol=ATOL_OUT, rtol=RTOL_OUT, err_msg=f"row {r}")
+
+
+def test_split_partials_vs_oracle(problem):
+    i, inp, dev = problem
+    if i not in (0, 1, 3):
+        pytest.skip("partials checked on workloads 0, 1, 3")
+    wl = inp["workload"]
+    rows = _rows(inp)
+    idx = dev.views["topk_idx"].cpu().numpy()
+    pm = dev.views["part_m"].cpu().numpy()
+    pl = dev.views["part_l"].cpu().numpy()
+    pa = dev.views["part_acc"].cpu().numpy()
+    q = O.bf16_bits_to_f64(inp["q"])
+    for r in _sample(i, rows)[:24]:
+        L = int(rows["row_len"][r])
+        sel = idx[r][idx[r] >= 0]
+        k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel) if L else (np.zeros((0, wl.num_kv_heads, wl.head_dim)),) * 2
+        m, l, acc = O.split_partials_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads, wl.num_splits)
+        fin = np.isfinite(m)
+        assert np.array_equal(fin, np.isfinite(pm[r])), r
+        np.testing.assert_allclose(pm[r][fin], m[fin], atol=ATOL_OUT, rtol=RTOL_OUT)
+        np.testing.assert_allclose(pl[r], l, atol=ATOL_OUT, rtol=RTOL_OUT)
+        np.testing.assert_allclose(pa[r], acc, atol=ATOL_OUT * 10, rtol=RTOL_OUT)
+
+
+def test_pad_rows_are_empty(problem):
+    i, inp, dev = problem
+    if i != 3:
+        pytest.skip("only workload 3 has pad rows")
+    n = dev.rows["num_rows"]
+    assert n == 560
+    assert (dev.views["topk_idx"][n:] == -1).all()
+    assert (dev.t["out"][n:].float() == 0).all()
+    assert torch.isneginf(dev.t["lse"][n:]).all()
+
+
+def test_step_equals_separate_calls_bitwise(problem, dsa_lib):
+    i, inp, dev = problem
+    cfg, t = dev.cfg, dev.t
+    ws = dsa_lib.alloc_workspace(cfg)
+    v = dsa_lib.workspace_views(cfg, ws)
+    out = torch.empty_like(t["out"])
+    lse = torch.empty_like(t["lse"])
+    dsa_lib.dsa_indexer_scores(cfg, t["q_idx"], t["w"], t["idx_cache"], t["idx_scale"], t["page_table"],
+                               t["row_req"], t["row_len"], t["block_first"], t["block_nrows"], v["scores"], ws)
+    dsa_lib.dsa_topk(cfg, v["scores"], t["row_len"], v["topk_idx"], ws)
+    dsa_lib.dsa_sparse_attn(cfg, t["q"], t["k_cache"], t["v_cache"], t["page_table"], t["row_req"], t["row_len"],
+                            v["topk_idx"], v["part_m"], v["part_l"], v["part_acc"], ws)
+    dsa_lib.dsa_merge(cfg, v["part_m"], v["part_l"], v["part_acc"], out, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(v["topk_idx"], dev.views["topk_idx"])
+    assert torch.equal(out.view(torch.int16), t["out"].view(torch.int16))
+    assert torch.equal(lse, t["lse"])
