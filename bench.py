@@ -48,11 +48,13 @@ CPU_SAMPLE_ROWS = 2
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["dsa", "reference"], default="dsa")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
     ap.add_argument("--splits", type=int, default=None, help="override the top-k split count")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="fewer decode requests (profiling captures only; the bench line uses the full batch)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-worker", default=None, help=argparse.SUPPRESS)
@@ -315,7 +317,11 @@ def run_dsa(args):
     from sparse_attention_decode_paged_gb300.harness import DeviceStep
 
     t_gen = time.time()
-    inp = W.generate(args.workload)
+    wl0 = W.workload(args.workload)
+    if args.batch:
+        import dataclasses
+        wl0 = dataclasses.replace(wl0, max_rows=args.batch, max_reqs=args.batch)
+    inp = W.generate(wl0)
     wl = inp["workload"]
     override = {"num_splits": args.splits} if args.splits else {}
     dev = DeviceStep(inp, **override)
@@ -425,7 +431,7 @@ def run_dsa(args):
         kernel_table[n]["frac_of_peak"] = kernel_table[n]["gbs"] / peak
 
     # ---- end to end through the public API, host buffers
-    e2e = run_e2e(args, dsa, dev, inp, stream, flush)
+    e2e = run_e2e(args, dsa, dev, inp, stream, flush) if args.e2e_steps > 0 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -213,8 +213,8 @@ def request_mix(wl: Workload):
         cache_len = rng.integers(512, 4096, size=8, endpoint=True).astype(np.int32)
         new = np.ones(8, dtype=np.int32)
     elif wl.seed == 2:
-        cache_len = np.full(64, 32768, dtype=np.int32)
-        new = np.ones(64, dtype=np.int32)
+        cache_len = np.full(wl.max_reqs, 32768, dtype=np.int32)
+        new = np.ones(wl.max_reqs, dtype=np.int32)
     elif wl.seed == 3:
         dec = rng.integers(1024, 32768, size=48, endpoint=True).astype(np.int32)
         cache_len = np.concatenate([dec, np.array([8192 + 512], dtype=np.int32)])
