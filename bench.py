@@ -43,6 +43,7 @@ DEFAULT_WORKLOAD = 2
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 CPU_SAMPLE_ROWS = 2
+KERNEL_SOURCE = {"indexer": "indexer_tc.cu", "sparse_attn": "attn.cu"}  # file holding each timed kernel
 
 
 def parse_args():
@@ -105,7 +106,7 @@ def traffic_record(kernel: str):
     with open(p) as f:
         d = json.load(f)
     rec = d.get(kernel)
-    if not rec:
+    if not rec or rec.get("source") != KERNEL_SOURCE.get(kernel):
         return None
     from sparse_attention_decode_paged_gb300 import build as B
     src = os.path.join(B.CSRC, rec["source"])

@@ -120,8 +120,7 @@ dsa_status_t dsa_validate_config(const dsa_config_t *c) {
     return fail(DSA_ERR_INVALID_ARG, "sm_scale must be positive and finite");
   if (static_cast<long long>(c->max_reqs) * c->max_pages_per_req > 0x7FFFFFFFLL)
     return fail(DSA_ERR_INVALID_ARG, "page table larger than 2^31 entries");
-  if (static_cast<long long>(c->max_rows) * 65536 > 0x7FFFFFFFLL)
-    return fail(DSA_ERR_INVALID_ARG, "max_rows too large");
+  if (c->max_rows > 4096) return fail(DSA_ERR_UNSUPPORTED, "max_rows %d > 4096", c->max_rows);
   return ok();
 }
 
@@ -243,6 +242,7 @@ dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, cons
   p.scores = scores;
   p.status = status_word(workspace);
   p.idx_heads = cfg->idx_heads;
+  p.idx_dim = cfg->idx_dim;
   p.max_rows = cfg->max_rows;
   p.max_reqs = cfg->max_reqs;
   p.max_pages_per_req = cfg->max_pages_per_req;
@@ -250,7 +250,7 @@ dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, cons
   p.num_pages = cfg->num_pages;
   p.page_size = cfg->page_size;
   p.block_rows = cfg->block_rows;
-  return cuda_status(dsa::launch_indexer(*cfg, p, stream), "indexer launch");
+  return cuda_status(dsa::launch_indexer_tc(*cfg, p, stream), "indexer launch");
 }
 
 dsa_status_t dsa_topk(const dsa_config_t *cfg, const float *scores, const int32_t *row_len,

@@ -20,7 +20,7 @@ struct IndexerParams {
   const int32_t *block_nrows;
   float *scores;            // [R, W]
   uint32_t *status;
-  int32_t idx_heads, max_rows, max_reqs, max_pages_per_req, score_width, num_pages;
+  int32_t idx_heads, idx_dim, max_rows, max_reqs, max_pages_per_req, score_width, num_pages;
   int32_t page_size, block_rows;
 };
 
@@ -58,6 +58,7 @@ struct MergeParams {
 
 // Each launcher returns the launch error (cudaSuccess when queued).
 cudaError_t launch_indexer(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st);
+cudaError_t launch_indexer_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st);
 cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, cudaStream_t st);
 cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cudaStream_t st);
 cudaError_t launch_merge(const dsa_config_t &cfg, const MergeParams &p, cudaStream_t st);

@@ -1,0 +1,576 @@
+// Lightning-indexer scores on the 5th-generation tensor cores (tcgen05 + TMA).
+//
+//   scores[r, t] = s_t * sum_h w[r, h] * max(0, q_idx[r, h, :] . k_t),  t < row_len[r]
+//
+// Megatron-LM PR #7211, commit message 1: the indexer streams page-contiguous
+// key tiles through tensor cores and each request's programs stride over its
+// row only up to its length; commit message 2: the rows of one score block are
+// scored against shared key tiles.
+//
+// Design (one persistent CTA per SM, 6 warps):
+//  * Work is the flat list of 128-token key tiles of all score blocks
+//    (block b contributes ceil(L_max(b) / 128) tiles).  Every CTA scans the
+//    block table, prefix-sums the tile counts and takes an equal contiguous
+//    range of tiles, so the launch depends only on the static config while
+//    the work follows the real lengths.
+//  * Warp 0 (producer): lane 0 streams each tile's pages with 2-D TMA loads
+//    (one box per page and 128-byte K atom, 128-byte swizzle) into a ring of
+//    shared-memory stages; when the score block changes, the whole warp
+//    stages the block's queries as the MMA's B operand (swizzled by hand; fp8
+//    keys: each query head is quantised to e4m3 with scale amax/448 and the
+//    scale is folded into the head weight, ReLU(s x) = s ReLU(x) for s > 0).
+//  * Warp 1 (MMA): one thread issues tcgen05.mma, transposed so that the key
+//    tile is A (M = 128 tokens) and the block's queries are B (N = 16..256
+//    heads x rows), accumulating in fp32 in tensor memory; two accumulator
+//    buffers let the epilogue of tile i overlap the MMAs of tile i+1.
+//  * Warps 2..5 (epilogue): thread i owns TMEM lane i = token i of the tile,
+//    reads its heads with tcgen05.ld, forms sum_h w_h ReLU(acc_h) with no
+//    cross-thread reduction, scales by s_t and stores the score.
+//  * Every wait is bounded; a wait that runs out sets DSA_DEV_TIMEOUT and an
+//    abort flag that releases the other roles, the producer waits for its
+//    copies in flight and the MMA warp for its MMAs, and TMEM is freed.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "dsa_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kTok = 128;  // tokens per key tile (MMA M)
+constexpr int kWarps = 6;  // 0 producer, 1 MMA, 2..5 epilogue
+constexpr int kThreads = kWarps * 32;
+constexpr long long kWaitBudget = 2000000000LL;  // SM cycles (about 1 s)
+constexpr int kMaxRowsTc = 4096;                  // prefix table capacity
+
+struct TcLayout {
+  int hp;         // indexer heads padded to a multiple of 16
+  int n_max;      // hp * block_rows: accumulator columns per buffer
+  int stages;     // key-tile ring depth
+  int nq;         // query buffers (1 or 2)
+  int tmem_cols;  // allocated TMEM columns (power of two >= 32)
+  uint32_t off_q, off_w, off_prefix, off_bar, off_misc;
+};
+
+template <int RB>
+__device__ __forceinline__ uint32_t swizzle(uint32_t off) {
+  constexpr uint32_t mask = RB == 128 ? 7u : (RB == 64 ? 3u : 1u);
+  return off ^ (((off >> 7) & mask) << 4);
+}
+
+template <int RB>
+__device__ __forceinline__ uint64_t make_desc(uint32_t saddr) {
+  constexpr uint64_t layout = RB == 128 ? 2u : (RB == 64 ? 4u : 6u);
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1u) << 16) |
+         (static_cast<uint64_t>((8u * RB) >> 4) << 32) | (static_cast<uint64_t>(1u) << 46) |
+         (layout << 61);
+}
+
+// Every lane of the warp waits (each acquires the barrier's phase); the
+// verdict is made warp-uniform so no lane continues alone.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int *abort_flag) {
+  const bool ok = tc::mbar_wait(bar, parity, abort_flag, kWaitBudget);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+struct BlockInfo {
+  int first, nrows, req, lmax;
+  int lens[4];
+};
+
+__device__ __forceinline__ BlockInfo load_block(const IndexerParams &p, int b) {
+  BlockInfo bi;
+  bi.first = p.block_first[b];
+  bi.nrows = p.block_nrows[b];
+  bi.req = p.row_req[bi.first];
+  bi.lmax = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    bi.lens[i] = i < bi.nrows ? p.row_len[bi.first + i] : 0;
+    bi.lmax = max(bi.lmax, bi.lens[i]);
+  }
+  return bi;
+}
+
+// Walks this CTA's contiguous range of tiles in order.
+struct Walker {
+  const int *prefix;
+  int item, end, block;
+  __device__ __forceinline__ void start(const int *pf, int nblocks, int beg, int e) {
+    prefix = pf;
+    item = beg;
+    end = e;
+    int lo = 0, hi = nblocks;  // find b with pf[b] <= beg < pf[b+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pf[mid] <= beg) lo = mid;
+      else hi = mid;
+    }
+    block = lo;
+    while (item < end && item >= prefix[block + 1]) ++block;
+  }
+  __device__ __forceinline__ bool valid() const { return item < end; }
+  __device__ __forceinline__ int tile() const { return item - prefix[block]; }
+  __device__ __forceinline__ bool last_of_block() const { return item + 1 >= prefix[block + 1] || item + 1 >= end; }
+  __device__ __forceinline__ void next() {
+    ++item;
+    while (item < end && item >= prefix[block + 1]) ++block;
+  }
+};
+
+template <int RB, int ATOMS, bool F8>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_tc_kernel(const IndexerParams p, const TcLayout lay, const __grid_constant__ CUtensorMap kmap) {
+  constexpr int kElem = F8 ? 1 : 2;
+  constexpr uint32_t kAtomB = kTok * RB;          // one K atom of a key tile
+  constexpr uint32_t kStageB = kAtomB * ATOMS;
+  constexpr int kKsteps = RB / 32;                // 32 bytes of K per MMA
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *sb = smem_raw + (base - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = lay.stages, NQ = lay.nq, HP = lay.hp, NMAX = lay.n_max;
+  const uint32_t qbufB = static_cast<uint32_t>(NMAX) * RB * ATOMS;
+  const uint32_t stage0 = base;
+  const uint32_t q0 = base + lay.off_q;
+  float *wbuf = reinterpret_cast<float *>(sb + lay.off_w);            // [NQ][NMAX]
+  int *prefix = reinterpret_cast<int *>(sb + lay.off_prefix);         // [R + 1]
+  const uint32_t bar0 = base + lay.off_bar;
+  // barrier map: full[S] empty[S] qfull[2] qempty[2] tfull[2] tempty[2] done
+  auto FULL = [&](int s) { return bar0 + 8u * s; };
+  auto EMPTY = [&](int s) { return bar0 + 8u * (S + s); };
+  auto QFULL = [&](int q) { return bar0 + 8u * (2 * S + q); };
+  auto QEMPTY = [&](int q) { return bar0 + 8u * (2 * S + 2 + q); };
+  auto TFULL = [&](int a) { return bar0 + 8u * (2 * S + 4 + a); };
+  auto TEMPTY = [&](int a) { return bar0 + 8u * (2 * S + 6 + a); };
+  const uint32_t DONE = bar0 + 8u * (2 * S + 8);
+  int *misc = reinterpret_cast<int *>(sb + lay.off_misc);  // [0] tmem base [1] abort [2..33] scan
+  volatile int *abort_flag = misc + 1;
+
+  // ---- tile counts per score block, prefix-summed (every CTA, redundantly)
+  const int R = p.max_rows;
+  for (int b = tid; b < R; b += kThreads) {
+    int nt = 0;
+    const int nrows = p.block_nrows[b];
+    if (nrows > 0) {
+      const int first = p.block_first[b];
+      bool ok = nrows <= p.block_rows && first >= 0 && first + nrows <= R;
+      const int req = ok ? p.row_req[first] : 0;
+      ok = ok && req >= 0 && req < p.max_reqs;
+      int lmax = 0;
+      for (int i = 0; i < nrows && ok; ++i) {
+        const int L = p.row_len[first + i];
+        if (p.row_req[first + i] != req || L < 0 || L > p.score_width) ok = false;
+        lmax = max(lmax, L);
+      }
+      if (!ok) {
+        if (blockIdx.x == 0) flag_status(p.status, DSA_DEV_BAD_BLOCK);
+      } else {
+        nt = (lmax + kTok - 1) / kTok;
+      }
+    }
+    prefix[b + 1] = nt;
+  }
+  if (tid == 0) {
+    prefix[0] = 0;
+    misc[1] = 0;
+  }
+  __syncthreads();
+  {
+    const int per = (R + kThreads - 1) / kThreads;
+    const int lo = 1 + tid * per, hi = min(R + 1, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += prefix[i];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) misc[2 + warp] = incl;
+    __syncthreads();
+    int run = incl - sum;
+    for (int w2 = 0; w2 < warp; ++w2) run += misc[2 + w2];
+    for (int i = lo; i < hi; ++i) {
+      run += prefix[i];
+      prefix[i] = run;
+    }
+    __syncthreads();
+  }
+  const int total = prefix[R];
+  const int beg = static_cast<int>((static_cast<long long>(blockIdx.x) * total) / gridDim.x);
+  const int end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total) / gridDim.x);
+  if (beg >= end) return;  // uniform across the CTA
+
+  // ---- barriers and tensor memory
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(FULL(s), 1);
+      tc::mbar_init(EMPTY(s), 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      tc::mbar_init(QFULL(q), 1);
+      tc::mbar_init(QEMPTY(q), 1 + 4);  // MMA commit + 4 epilogue warps
+      tc::mbar_init(TFULL(q), 1);
+      tc::mbar_init(TEMPTY(q), 4);
+    }
+    tc::mbar_init(DONE, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) tc::tma_prefetch_desc(&kmap);
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(&misc[0]), static_cast<uint32_t>(lay.tmem_cols));
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+
+  Walker wk;
+  wk.start(prefix, R, beg, end);
+
+  if (warp == 0) {
+    // ======================================================== producer
+    const uint64_t policy = tc::l2_evict_first_policy();
+    int cur = -1, qcount = -1, issued = 0;
+    BlockInfo bi{};
+    const int32_t *pt = nullptr;
+    for (; wk.valid(); wk.next()) {
+      if (wk.block != cur) {
+        cur = wk.block;
+        ++qcount;
+        bi = load_block(p, cur);
+        pt = p.page_table + static_cast<size_t>(bi.req) * p.max_pages_per_req;
+        const int qb = qcount % NQ;
+        if (!warp_wait(QEMPTY(qb), ((qcount / NQ) & 1) ^ 1, abort_flag)) {
+          if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+          break;
+        }
+        // stage the block's queries (B operand) and head weights
+        uint8_t *qdst = sb + lay.off_q + qb * qbufB;
+        float *wdst = wbuf + qb * NMAX;
+        const int DIr = p.idx_dim;  // real dim (<= kDI)
+        for (int n = lane; n < NMAX; n += 32) {
+          const int rr = n / HP, h = n % HP;
+          const bool live = rr < bi.nrows && h < p.idx_heads;
+          const uint8_t *src = p.q_idx + (static_cast<size_t>(bi.first + rr) * p.idx_heads + h) * DIr * 2;
+          float sigma = 1.f;
+          if constexpr (F8) {
+            float amax = 0.f;
+            if (live)
+              for (int d = 0; d < DIr; d += 8) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(src + d * 2);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))),
+                                         fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y)))));
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v.z)), fabsf(bf16hi(v.z))),
+                                         fmaxf(fabsf(bf16lo(v.w)), fabsf(bf16hi(v.w)))));
+              }
+            sigma = amax > 0.f ? amax / 448.f : 1.f;
+            const float inv = 1.f / sigma;
+            for (int a = 0; a < ATOMS; ++a)
+              for (int c = 0; c < RB / 16; ++c) {  // 16 e4m3 per chunk
+                uint32_t o[4] = {0u, 0u, 0u, 0u};
+                const int d0 = a * RB + c * 16;
+                if (live && d0 < DIr) {
+                  const uint4 v0 = *reinterpret_cast<const uint4 *>(src + d0 * 2);
+                  const uint4 v1 = *reinterpret_cast<const uint4 *>(src + d0 * 2 + 16);
+                  const uint32_t w8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                  for (int k = 0; k < 8; ++k) {
+                    const __nv_fp8x2_storage_t pr = __nv_cvt_float2_to_fp8x2(
+                        make_float2(bf16lo(w8[k]) * inv, bf16hi(w8[k]) * inv), __NV_SATFINITE, __NV_E4M3);
+                    o[k >> 1] |= static_cast<uint32_t>(pr) << (16 * (k & 1));
+                  }
+                }
+                *reinterpret_cast<uint4 *>(qdst + a * NMAX * RB + swizzle<RB>(n * RB + c * 16)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+              }
+          } else {
+            for (int a = 0; a < ATOMS; ++a)
+              for (int c = 0; c < RB / 16; ++c) {  // 8 bf16 per chunk
+                const int d0 = a * (RB / 2) + c * 8;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (live && d0 < DIr) v = *reinterpret_cast<const uint4 *>(src + d0 * 2);
+                *reinterpret_cast<uint4 *>(qdst + a * NMAX * RB + swizzle<RB>(n * RB + c * 16)) = v;
+              }
+          }
+          wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] * sigma : 0.f;
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(QFULL(qb));
+      }
+      if (lane == 0) {
+        const int it = wk.item - beg;
+        const int s = it % S;
+        if (!tc::mbar_wait(EMPTY(s), ((it / S) & 1) ^ 1, abort_flag, kWaitBudget)) {
+          *abort_flag = 1;
+          flag_status(p.status, DSA_DEV_TIMEOUT);
+        } else {
+          const int t0 = wk.tile() * kTok;
+          const int P = p.page_size;
+          const int npg = kTok / P;
+          int pages[8];
+          int nvalid = 0;
+          for (int k = 0; k < npg; ++k) {
+            const int t = t0 + k * P;
+            pages[k] = -1;
+            if (t < bi.lmax) {
+              const int pg = pt[t / P];
+              if (pg >= 0 && pg < p.num_pages) {
+                pages[k] = pg;
+                ++nvalid;
+              } else {
+                flag_status(p.status, DSA_DEV_BAD_PAGE);
+              }
+            }
+          }
+          tc::mbar_arrive_expect_tx(FULL(s), static_cast<uint32_t>(nvalid) * P * RB * ATOMS);
+          for (int k = 0; k < npg; ++k) {
+            if (pages[k] < 0) continue;
+#pragma unroll
+            for (int a = 0; a < ATOMS; ++a)
+              tc::tma_load_2d(stage0 + s * kStageB + a * kAtomB + k * P * RB, &kmap, a * (RB / kElem),
+                              pages[k] * P, FULL(s), policy);
+          }
+          ++issued;
+        }
+      }
+      __syncwarp();
+      if (__shfl_sync(0xFFFFFFFFu, *abort_flag, 0)) break;
+    }
+    // no copy may land after the CTA exits: wait for the last stages issued
+    if (lane == 0)
+      for (int it = max(0, issued - S); it < issued; ++it)
+        tc::mbar_wait(FULL(it % S), (it / S) & 1, nullptr, kWaitBudget);
+    __syncwarp();
+  } else if (warp == 1) {
+    // ============================================================ MMA
+    if (lane == 0) {
+      int cur = -1, qcount = -1, qb = 0, nrows = 1;
+      bool any = false;
+      for (; wk.valid(); wk.next()) {
+        const int it = wk.item - beg;
+        const int s = it % S, ab = it & 1;
+        if (wk.block != cur) {
+          cur = wk.block;
+          ++qcount;
+          qb = qcount % NQ;
+          nrows = p.block_nrows[cur];
+          if (!tc::mbar_wait(QFULL(qb), (qcount / NQ) & 1, abort_flag, kWaitBudget)) break;
+        }
+        if (!tc::mbar_wait(TEMPTY(ab), ((it >> 1) & 1) ^ 1, abort_flag, kWaitBudget)) break;
+        if (!tc::mbar_wait(FULL(s), (it / S) & 1, abort_flag, kWaitBudget)) break;
+        tc::tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(ab * NMAX);
+        const uint32_t idesc = tc::idesc_m128(HP * nrows, F8);
+#pragma unroll
+        for (int a = 0; a < ATOMS; ++a)
+#pragma unroll
+          for (int k = 0; k < kKsteps; ++k) {
+            const uint64_t ad = make_desc<RB>(stage0 + s * kStageB + a * kAtomB + k * 32);
+            const uint64_t bd = make_desc<RB>(q0 + qb * qbufB + a * NMAX * RB + k * 32);
+            tc::mma<F8>(d, ad, bd, idesc, (a | k) != 0 ? 1u : 0u);
+          }
+        tc::mma_commit(EMPTY(s));
+        tc::mma_commit(TFULL(ab));
+        if (wk.last_of_block()) tc::mma_commit(QEMPTY(qb));
+        any = true;
+      }
+      if (wk.valid()) {
+        *abort_flag = 1;
+        flag_status(p.status, DSA_DEV_TIMEOUT);
+      }
+      if (any) {  // every MMA issued here has completed before TMEM is freed
+        tc::mma_commit(DONE);
+        tc::mbar_wait(DONE, 0, nullptr, kWaitBudget);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ======================================================= epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int tl = quarter * 32 + lane;
+    int cur = -1, qcount = -1, qb = 0;
+    BlockInfo bi{};
+    const int32_t *pt = nullptr;
+    for (; wk.valid(); wk.next()) {
+      const int it = wk.item - beg;
+      const int ab = it & 1;
+      if (wk.block != cur) {
+        if (cur >= 0 && lane == 0) tc::mbar_arrive(QEMPTY(qb));  // done with the old weights
+        cur = wk.block;
+        ++qcount;
+        qb = qcount % NQ;
+        bi = load_block(p, cur);
+        pt = p.page_table + static_cast<size_t>(bi.req) * p.max_pages_per_req;
+        if (!warp_wait(QFULL(qb), (qcount / NQ) & 1, abort_flag)) {
+          if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+          break;
+        }
+      }
+      if (!warp_wait(TFULL(ab), (it >> 1) & 1, abort_flag)) {
+        if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+        break;
+      }
+      tc::tc_fence_after();
+      const int t = wk.tile() * kTok + tl;
+      float sc = 1.f;
+      if constexpr (F8) {
+        sc = 0.f;
+        if (t < bi.lmax) {
+          const int pg = pt[t / p.page_size];
+          if (pg >= 0 && pg < p.num_pages)
+            sc = p.idx_scale[static_cast<size_t>(pg) * p.page_size + t % p.page_size];
+        }
+      }
+      const float *wq = wbuf + qb * NMAX;
+      const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(ab * NMAX);
+      for (int rr = 0; rr < bi.nrows; ++rr) {
+        float sum = 0.f;
+        for (int c = 0; c < HP; c += 16) {
+          float v[16];
+          tc::tmem_ld16_sync(trow + rr * HP + c, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sum = fmaf(wq[rr * HP + c + i], fmaxf(v[i], 0.f), sum);
+        }
+        int L = bi.lens[0];
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+          if (rr == i) L = bi.lens[i];
+        if (t < L) p.scores[static_cast<size_t>(bi.first + rr) * p.score_width + t] = sum * sc;
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(TEMPTY(ab));
+    }
+  }
+
+  // ---- teardown: every role is out of its loop and its async work is done
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, static_cast<uint32_t>(lay.tmem_cols));
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+constexpr int kSmemLimit = 232448;  // 227 KiB of dynamic shared memory per CTA
+constexpr int kSmemFloor = 120 * 1024;  // keeps one CTA (and one TMEM owner) per SM
+
+template <int RB, int ATOMS, bool F8>
+cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st) {
+  constexpr int kElem = F8 ? 1 : 2;
+  auto encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  TcLayout lay;
+  lay.hp = (cfg.idx_heads + 15) & ~15;
+  lay.n_max = lay.hp * cfg.block_rows;
+  if (lay.n_max > 256 || cfg.max_rows > kMaxRowsTc) return cudaErrorInvalidValue;
+  int cols = 32;
+  while (cols < 2 * lay.n_max) cols <<= 1;
+  lay.tmem_cols = cols;
+  const uint32_t stageB = kTok * RB * ATOMS;
+  const uint32_t qbufB = static_cast<uint32_t>(lay.n_max) * RB * ATOMS;
+  auto fixed = [&](int nq) {
+    uint32_t off = nq * qbufB;                    // query buffers (after the stages)
+    off += nq * lay.n_max * 4;                    // weights
+    off += (cfg.max_rows + 1) * 4 + 8;            // prefix table
+    off += (2 * 8 + 9) * 8 + 64;                  // barriers (upper bound) + misc
+    return off + 1024 + 34 * 4;                   // alignment slack, scan scratch
+  };
+  lay.nq = 2;
+  int stages = static_cast<int>((kSmemLimit - fixed(2)) / stageB);
+  if (stages < 4) {
+    lay.nq = 1;
+    stages = static_cast<int>((kSmemLimit - fixed(1)) / stageB);
+  }
+  stages = stages > 8 ? 8 : stages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  lay.stages = stages;
+  uint32_t off = stages * stageB;
+  lay.off_q = off;
+  off += lay.nq * qbufB;
+  lay.off_w = off;
+  off += lay.nq * lay.n_max * 4;
+  lay.off_prefix = off;
+  off += (cfg.max_rows + 1) * 4;
+  off = (off + 7u) & ~7u;
+  lay.off_bar = off;
+  off += (2 * stages + 9) * 8;
+  lay.off_misc = off;
+  off += 34 * 4;
+  size_t smem = off + 1024;
+  if (smem < static_cast<size_t>(kSmemFloor)) smem = kSmemFloor;
+  if (smem > static_cast<size_t>(kSmemLimit)) return cudaErrorInvalidValue;
+
+  CUtensorMap kmap;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cfg.idx_dim),
+                              static_cast<cuuint64_t>(cfg.num_pages) * cfg.page_size};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cfg.idx_dim) * kElem};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(RB / kElem), static_cast<cuuint32_t>(cfg.page_size)};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUtensorMapSwizzle swz = RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : RB == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                            : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult cr = encode(&kmap, F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                       const_cast<uint8_t *>(p.idx_cache), gdim, gstride, box, estride,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<RB, ATOMS, F8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = sm_count();
+  if (grid <= 0) return cudaErrorNoDevice;
+  indexer_tc_kernel<RB, ATOMS, F8><<<grid, kThreads, smem, st>>>(p, lay, kmap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st) {
+  const bool f8 = cfg.idx_key_dtype == DSA_KEY_FP8_E4M3;
+  if (f8) {
+    switch (cfg.idx_dim) {
+      case 32: return launch_tc<32, 1, true>(cfg, p, st);
+      case 64: return launch_tc<64, 1, true>(cfg, p, st);
+      case 128: return launch_tc<128, 1, true>(cfg, p, st);
+    }
+  } else {
+    switch (cfg.idx_dim) {
+      case 32: return launch_tc<64, 1, false>(cfg, p, st);
+      case 64: return launch_tc<128, 1, false>(cfg, p, st);
+      case 128: return launch_tc<128, 2, false>(cfg, p, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dsa

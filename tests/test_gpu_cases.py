@@ -37,7 +37,13 @@ def test_indexer_exact_on_integer_inputs(fp8, dsa_lib, cuda_ok):
     inp = W.generate(wl)
     rng = np.random.default_rng(21)
     R, HI, DI = wl.max_rows, wl.idx_heads, wl.idx_dim
-    inp["q_idx"] = _bf16_bits_of(rng.integers(-3, 4, (R, HI, DI)))
+    q = rng.integers(-3, 4, (R, HI, DI)).astype(np.float32)
+    if fp8:
+        # fp8 keys: the kernel quantises each query head to e4m3 with scale
+        # amax/448; a head whose largest entry is 448 has scale 1 and small
+        # integers are e4m3 values, so that quantisation is lossless here
+        q[..., 0] = 448.0
+    inp["q_idx"] = _bf16_bits_of(q)
     inp["w"] = (2.0 ** rng.integers(-2, 2, (R, HI)) * rng.choice([-1.0, 1.0], (R, HI))).astype(np.float32)
     keys = rng.integers(-4, 5, inp["idx_cache"].shape).astype(np.float32)
     if fp8:
