@@ -80,7 +80,7 @@ typedef enum { DSA_KEY_BF16 = 0, DSA_KEY_FP8_E4M3 = 1 } dsa_key_dtype_t;
  * Model shape and static capacity; fixed for the lifetime of a captured
  * graph.  Supported by this build:
  *   num_q_heads % num_kv_heads == 0, num_q_heads / num_kv_heads <= 8,
- *   num_kv_heads <= 16, head_dim in {64, 128};
+ *   num_kv_heads <= 8, head_dim in {64, 128}, max_rows <= 4096;
  *   1 <= idx_heads <= 64, idx_dim in {32, 64, 128};
  *   page_size in {16, 32, 64, 128}; 1 <= block_rows <= 4;
  *   1 <= topk <= score_width <= max_pages_per_req * page_size;

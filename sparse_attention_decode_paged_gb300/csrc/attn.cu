@@ -5,29 +5,36 @@
 // top-k slots are split across programs whose slices are merged flash-decoding
 // style; commit message 8: probabilities enter the value reduction in fp32.
 //
-// sparse_attn_kernel: grid (S splits, R rows), one warp per KV head g.  The
-// warp walks its split's slots 16 at a time: lanes 0..15 resolve slot ->
-// position -> page -> row offset (bounds-checked), every lane issues its
-// 16-byte loads of two K rows (scores) and 8-byte loads of all 16 V rows
-// before any arithmetic, so 8 KiB per warp are in flight.  Scores use the
-// tensor cores (mma.sync m16n8k16, A = 16 keys x 16 dims, B = the group's <= 8
-// query heads) with the head dim permuted identically on both operands so
-// each lane's key bytes are one contiguous 16-byte load.  The online softmax
-// runs in the log2 domain in fp32; p (fp32, never rounded) and the rescale
-// factors go through shared memory and every lane accumulates its 4 (D=128)
-// or 2 (D=64) value dims for all heads with fp32 FMA.
+// sparse_attn_kernel: persistent CTAs walk the (row, split) work items.  Warp
+// 0 is the gather producer: its lanes resolve 8 selected slots at a time
+// (slot -> position -> page -> row offset, bounds-checked) and issue one
+// cp.async.bulk per token for its K row and one for its V row (all KV heads
+// of a token are contiguous, Hkv*D*2 bytes), into a ring of shared-memory
+// stages that complete on mbarriers.  Warps 1..Hkv are consumers, one per KV
+// head g: scores on the tensor cores (mma.sync m16n8k16 with the group's <= 8
+// query heads as the A rows and 8 keys as N; key fragments by ldmatrix from
+// rows padded by 16 bytes so the 8 rows hit distinct banks), an online
+// softmax in the log2 domain in fp32, and the value reduction with fp32
+// probabilities and fp32 FMA (each lane owns D/32 value dims of all heads).
+// Bytes in flight are set by the ring depth, not by registers.  Every wait is
+// bounded by an SM-clock budget; a wait that runs out sets DSA_DEV_TIMEOUT.
 //
 // merge_kernel: one warp per (row, head); combines the S partial states.
 #include <math.h>
 
+#include <algorithm>
+
 #include "dsa_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kChunk = 16;       // selected keys per warp iteration
-constexpr int kMaxKvHeads = 16;  // warps per CTA
+constexpr int kTokA = 8;         // selected keys per stage
+constexpr int kMaxKvHeads = 8;  // consumer warps per CTA
+constexpr int kMaxStagesA = 6;
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr long long kWaitBudgetA = 2000000000LL;  // SM cycles (about 1 s)
 
 template <int D>
 struct VecV;
@@ -35,203 +42,253 @@ template <>
 struct VecV<128> {
   using T = uint2;  // 4 bf16
   static constexpr int kN = 4;
-  __device__ __forceinline__ static T load(const uint8_t *p) { return ldg_nc_v2(p); }
   __device__ __forceinline__ static void unpack(const T &v, float (&f)[4]) {
     f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
   }
-  __device__ __forceinline__ static T zero() { return make_uint2(0u, 0u); }
 };
 template <>
 struct VecV<64> {
   using T = uint32_t;  // 2 bf16
   static constexpr int kN = 2;
-  __device__ __forceinline__ static T load(const uint8_t *p) {
-    uint32_t r;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];\n" : "=r"(r) : "l"(p));
-    return r;
-  }
   __device__ __forceinline__ static void unpack(const T &v, float (&f)[2]) {
     f[0] = bf16lo(v); f[1] = bf16hi(v);
   }
-  __device__ __forceinline__ static T zero() { return 0u; }
 };
 
-template <int D>
-__global__ void __launch_bounds__(32 * kMaxKvHeads) sparse_attn_kernel(const AttnParams p) {
-  using V = VecV<D>;
-  constexpr int KJ = D / 32;  // 16-byte pieces of a key row per lane quad
-  constexpr int VN = V::kN;   // value dims per lane
-  __shared__ float p_s[kMaxKvHeads][kChunk][8];
-  __shared__ float a_s[kMaxKvHeads][8];
+struct AttnLayout {
+  int stages;
+  int row_bytes;  // Hkv * D * 2: one token's K (or V) row, all KV heads
+  int row_pitch;  // row_bytes + 16 in shared memory
+  uint32_t off_ok, off_p, off_a, off_bar, off_misc;
+};
 
-  const int s = blockIdx.x, r = blockIdx.y;
-  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c4 = lane & 3, g4 = lane >> 2;
-  const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv, S = p.num_splits;
-  const int K = p.topk, P = p.page_size;
+struct RowSplit {
+  int r, s, L, req, a, b;
+};
 
-  int L = p.row_len[r];
-  const int req = p.row_req[r];
-  const bool row_ok = L >= 0 && L <= p.score_width && (L == 0 || (req >= 0 && req < p.max_reqs));
-  if (!row_ok) {
-    if (lane == 0) flag_status(p.status, DSA_DEV_BAD_ROW);
+__device__ __forceinline__ RowSplit row_split(const AttnParams &p, int item, bool flag) {
+  RowSplit x;
+  x.r = item / p.num_splits;
+  x.s = item % p.num_splits;
+  int L = p.row_len[x.r];
+  const int req = p.row_req[x.r];
+  const bool ok = L >= 0 && L <= p.score_width && (L == 0 || (req >= 0 && req < p.max_reqs));
+  if (!ok) {
+    if (flag) flag_status(p.status, DSA_DEV_BAD_ROW);
     L = 0;
   }
-  const int n = min(K, L);
-  const int a = static_cast<int>((static_cast<long long>(s) * n) / S);
-  const int b = static_cast<int>((static_cast<long long>(s + 1) * n) / S);
+  x.L = L;
+  x.req = L > 0 ? req : 0;
+  const int n = min(p.topk, L);
+  x.a = static_cast<int>((static_cast<long long>(x.s) * n) / p.num_splits);
+  x.b = static_cast<int>((static_cast<long long>(x.s + 1) * n) / p.num_splits);
+  return x;
+}
 
-  // query heads of this group as the B operand (dims permuted, see header)
-  uint4 qf[KJ];
-#pragma unroll
-  for (int j = 0; j < KJ; ++j) {
-    qf[j] = make_uint4(0u, 0u, 0u, 0u);
-    if (g4 < G)
-      qf[j] = *reinterpret_cast<const uint4 *>(
-          p.q + ((static_cast<size_t>(r) * Hq + g * G + g4) * D + 32 * j + 8 * c4) * 2);
+__device__ __forceinline__ bool warp_wait_a(uint32_t bar, uint32_t parity, const volatile int *abort_flag) {
+  const bool ok = tc::mbar_wait(bar, parity, abort_flag, kWaitBudgetA);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * (1 + kMaxKvHeads)) sparse_attn_kernel(const AttnParams p,
+                                                                              const AttnLayout lay) {
+  using V = VecV<D>;
+  constexpr int VN = V::kN;  // value dims per lane
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv, S = p.num_splits;
+  const int NST = lay.stages, pitch = lay.row_pitch;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t stageB = 2u * kTokA * pitch;                      // K block then V block
+  int *tok_ok = reinterpret_cast<int *>(smem + lay.off_ok);        // [NST][kTokA]
+  float *p_s = reinterpret_cast<float *>(smem + lay.off_p);        // [Hkv][kTokA][8]
+  float *a_s = reinterpret_cast<float *>(smem + lay.off_a);        // [Hkv][8]
+  const uint32_t bar0 = sbase + lay.off_bar;
+  auto FULL = [&](int st) { return bar0 + 8u * st; };
+  auto EMPTY = [&](int st) { return bar0 + 8u * (NST + st); };
+  volatile int *abort_flag = reinterpret_cast<int *>(smem + lay.off_misc);
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NST; ++st) {
+      tc::mbar_init(FULL(st), 1);
+      tc::mbar_init(EMPTY(st), Hkv);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
   }
+  __syncthreads();
 
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2c4, 2c4+1 (log2 domain)
-  float acc[8][VN];
+  const int items = p.max_rows_attn * S;
+  const long long tok_stride = static_cast<long long>(Hkv) * D;  // elements per token row
+
+  if (warp == 0) {
+    // ====================================================== gather producer
+    const uint64_t policy = tc::l2_evict_first_policy();
+    int chunk = 0;  // global chunk counter (ring position)
+    bool stop = false;
+    for (int item = blockIdx.x; item < items && !stop; item += gridDim.x) {
+      const RowSplit x = row_split(p, item, lane == 0);
+      const int32_t *sel = p.topk_idx + static_cast<size_t>(x.r) * p.topk;
+      const int32_t *pt = p.page_table + static_cast<size_t>(x.req) * p.max_pages_per_req;
+      for (int base = x.a; base < x.b; base += kTokA, ++chunk) {
+        const int st = chunk % NST;
+        if (!warp_wait_a(EMPTY(st), ((chunk / NST) & 1) ^ 1, abort_flag)) {
+          if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+          stop = true;
+          break;
+        }
+        long long off = -1;  // element offset of the token row
+        if (lane < kTokA) {
+          const int i = base + lane;
+          if (i < x.b) {
+            const int t = sel[i];
+            if (t != -1) {
+              if (t < 0 || t >= x.L) {
+                flag_status(p.status, DSA_DEV_BAD_INDEX);
+              } else {
+                const int page = pt[t / p.page_size];
+                if (page < 0 || page >= p.num_pages)
+                  flag_status(p.status, DSA_DEV_BAD_PAGE);
+                else
+                  off = (static_cast<long long>(page) * p.page_size + (t % p.page_size)) * tok_stride;
+              }
+            }
+          }
+          tok_ok[st * kTokA + lane] = off >= 0 ? 1 : 0;
+        }
+        const uint32_t valid = __ballot_sync(0xFFFFFFFFu, off >= 0);
+        __syncwarp();
+        if (lane == 0)
+          tc::mbar_arrive_expect_tx(FULL(st), static_cast<uint32_t>(__popc(valid)) * 2u * lay.row_bytes);
+        __syncwarp();
+        if (off >= 0) {
+          const uint32_t dk = sbase + st * stageB + lane * pitch;
+          tc::bulk_load(dk, p.k_cache + off * 2, lay.row_bytes, FULL(st), policy);
+          tc::bulk_load(dk + kTokA * pitch, p.v_cache + off * 2, lay.row_bytes, FULL(st), policy);
+        }
+      }
+    }
+    // drain: no copy may land after the CTA exits
+    if (lane == 0)
+      for (int c = max(0, chunk - NST); c < chunk; ++c)
+        tc::mbar_wait(FULL(c % NST), (c / NST) & 1, nullptr, kWaitBudgetA);
+    __syncwarp();
+  } else if (warp <= Hkv) {
+    // ============================================ consumers: one per KV head
+    const int g = warp - 1;
+    const int c4 = lane & 3, g4 = lane >> 2;  // g4: query head of the group (A row)
+    float *pw = p_s + g * kTokA * 8;
+    float *aw = a_s + g * 8;
+    int chunk = 0;
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+      const RowSplit x = row_split(p, item, false);
+      // A operand: this group's query heads (rows 8..15 are zero padding)
+      uint32_t qa[D / 16][2];
 #pragma unroll
-  for (int h = 0; h < 8; ++h)
+      for (int ks = 0; ks < D / 16; ++ks) {
+        qa[ks][0] = qa[ks][1] = 0u;
+        if (g4 < G) {
+          const uint8_t *qrow = p.q + ((static_cast<size_t>(x.r) * Hq + g * G + g4) * D + ks * 16 + 2 * c4) * 2;
+          qa[ks][0] = *reinterpret_cast<const uint32_t *>(qrow);
+          qa[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16);
+        }
+      }
+      float m = -INFINITY, l = 0.f;  // head g4, log2 domain
+      float acc[8][VN];
 #pragma unroll
-    for (int d = 0; d < VN; ++d) acc[h][d] = 0.f;
-
-  const int32_t *sel = p.topk_idx + static_cast<size_t>(r) * K;
-  const int32_t *pt =
-      p.page_table + static_cast<size_t>(L > 0 ? req : 0) * p.max_pages_per_req;
-  const long long tok_stride = static_cast<long long>(Hkv) * D;  // elements per token
-
-  for (int base = a; base < b; base += kChunk) {
-    long long off = -1;  // element offset of row (t, g) in the caches; -1 = skip
-    if (lane < kChunk) {
-      const int i = base + lane;
-      if (i < b) {
-        const int t = sel[i];
-        if (t != -1) {
-          if (t < 0 || t >= L) {
-            flag_status(p.status, DSA_DEV_BAD_INDEX);
+      for (int h = 0; h < 8; ++h)
+#pragma unroll
+        for (int d = 0; d < VN; ++d) acc[h][d] = 0.f;
+      bool aborted = false;
+      for (int base = x.a; base < x.b; base += kTokA, ++chunk) {
+        const int st = chunk % NST;
+        if (!warp_wait_a(FULL(st), (chunk / NST) & 1, abort_flag)) {
+          if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+          aborted = true;
+          break;
+        }
+        const uint32_t kst = sbase + st * stageB;
+        const int *ok = tok_ok + st * kTokA;
+        // S[head][token] = Q . K^T over D
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const int tok = lane & 7, mat = lane >> 3;
+          const uint32_t kaddr = kst + tok * pitch + (g * D + (mat >> 1) * 16 + (mat & 1) * 8) * 2;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ks += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(kaddr + ks * 32, b0, b1, b2, b3);
+            mma_bf16_16816(c, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+            mma_bf16_16816(c, qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, b2, b3);
+          }
+        }
+        const bool v0 = ok[2 * c4] != 0, v1 = ok[2 * c4 + 1] != 0;
+        const float x0 = v0 ? c[0] * p.sm_scale_log2 : -INFINITY;
+        const float x1 = v1 ? c[1] * p.sm_scale_log2 : -INFINITY;
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const float mn = fmaxf(m, mx);
+        const float al = mn == -INFINITY ? 1.f : exp2f(m - mn);
+        const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - mn);
+        const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - mn);
+        float ps = p0 + p1;
+        ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
+        ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
+        l = l * al + ps;
+        m = mn;
+        pw[(2 * c4) * 8 + g4] = p0;
+        pw[(2 * c4 + 1) * 8 + g4] = p1;
+        if (c4 == 0) aw[g4] = al;
+        __syncwarp();
+        {
+          const float4 alo = *reinterpret_cast<const float4 *>(aw);
+          const float4 ahi = *reinterpret_cast<const float4 *>(aw + 4);
+          const float alv[8] = {alo.x, alo.y, alo.z, alo.w, ahi.x, ahi.y, ahi.z, ahi.w};
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+#pragma unroll
+            for (int d = 0; d < VN; ++d) acc[h][d] *= alv[h];
+        }
+        const uint8_t *vbase = smem + st * stageB + kTokA * pitch + (g * D + lane * VN) * 2;
+#pragma unroll
+        for (int j = 0; j < kTokA; ++j) {
+          if (!ok[j]) continue;
+          const float4 plo = *reinterpret_cast<const float4 *>(pw + j * 8);
+          const float4 phi = *reinterpret_cast<const float4 *>(pw + j * 8 + 4);
+          const float pv[8] = {plo.x, plo.y, plo.z, plo.w, phi.x, phi.y, phi.z, phi.w};
+          float vf[VN];
+          V::unpack(*reinterpret_cast<const typename V::T *>(vbase + j * pitch), vf);
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+#pragma unroll
+            for (int d = 0; d < VN; ++d) acc[h][d] = fmaf(pv[h], vf[d], acc[h][d]);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(EMPTY(st));
+      }
+      if (aborted) break;
+      // partial state of heads g*G .. g*G+G-1 for this split
+      const size_t rh0 = static_cast<size_t>(x.r) * Hq + static_cast<size_t>(g) * G;
+      if (c4 == 0 && g4 < G) {
+        p.part_m[(rh0 + g4) * S + x.s] = m == -INFINITY ? -INFINITY : m * kLn2;
+        p.part_l[(rh0 + g4) * S + x.s] = l;
+      }
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        if (h < G) {
+          float *dst = p.part_acc + ((rh0 + h) * S + x.s) * D + lane * VN;
+          if constexpr (VN == 4) {
+            *reinterpret_cast<float4 *>(dst) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
           } else {
-            const int page = pt[t / P];
-            if (page < 0 || page >= p.num_pages)
-              flag_status(p.status, DSA_DEV_BAD_PAGE);
-            else
-              off = (static_cast<long long>(page) * P + (t % P)) * tok_stride +
-                    static_cast<long long>(g) * D;
+            *reinterpret_cast<float2 *>(dst) = make_float2(acc[h][0], acc[h][1]);
           }
         }
       }
     }
-    const long long ok0 = __shfl_sync(0xFFFFFFFFu, off, g4);
-    const long long ok1 = __shfl_sync(0xFFFFFFFFu, off, g4 + 8);
-    uint4 kf0[KJ], kf1[KJ];
-#pragma unroll
-    for (int j = 0; j < KJ; ++j) {
-      kf0[j] = ok0 >= 0 ? ldg_nc_v4(p.k_cache + (ok0 + 32 * j + 8 * c4) * 2) : make_uint4(0u, 0u, 0u, 0u);
-      kf1[j] = ok1 >= 0 ? ldg_nc_v4(p.k_cache + (ok1 + 32 * j + 8 * c4) * 2) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    typename V::T vv[kChunk];
-    bool vok[kChunk];
-#pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      const long long ov = __shfl_sync(0xFFFFFFFFu, off, i);
-      vok[i] = ov >= 0;
-      vv[i] = vok[i] ? V::load(p.v_cache + (ov + lane * VN) * 2) : V::zero();
-    }
-
-    // scores S^T[token][head] = K . Q^T
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < KJ; ++j) {
-      mma_bf16_16816(c, kf0[j].x, kf1[j].x, kf0[j].y, kf1[j].y, qf[j].x, qf[j].y);
-      mma_bf16_16816(c, kf0[j].z, kf1[j].z, kf0[j].w, kf1[j].w, qf[j].z, qf[j].w);
-    }
-    const float x0 = ok0 >= 0 ? c[0] * p.sm_scale_log2 : -INFINITY;
-    const float x1 = ok0 >= 0 ? c[1] * p.sm_scale_log2 : -INFINITY;
-    const float x2 = ok1 >= 0 ? c[2] * p.sm_scale_log2 : -INFINITY;
-    const float x3 = ok1 >= 0 ? c[3] * p.sm_scale_log2 : -INFINITY;
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-    const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - mn0);
-    const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - mn1);
-    const float p2 = x2 == -INFINITY ? 0.f : exp2f(x2 - mn0);
-    const float p3 = x3 == -INFINITY ? 0.f : exp2f(x3 - mn1);
-    float ps0 = p0 + p2, ps1 = p1 + p3;
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, o);
-      ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, o);
-    }
-    l0 = l0 * al0 + ps0;
-    l1 = l1 * al1 + ps1;
-    m0 = mn0;
-    m1 = mn1;
-    p_s[g][g4][2 * c4] = p0;
-    p_s[g][g4][2 * c4 + 1] = p1;
-    p_s[g][g4 + 8][2 * c4] = p2;
-    p_s[g][g4 + 8][2 * c4 + 1] = p3;
-    if (g4 == 0) {
-      a_s[g][2 * c4] = al0;
-      a_s[g][2 * c4 + 1] = al1;
-    }
-    __syncwarp();
-    {
-      const float4 alo = *reinterpret_cast<const float4 *>(&a_s[g][0]);
-      const float4 ahi = *reinterpret_cast<const float4 *>(&a_s[g][4]);
-      const float al[8] = {alo.x, alo.y, alo.z, alo.w, ahi.x, ahi.y, ahi.z, ahi.w};
-#pragma unroll
-      for (int h = 0; h < 8; ++h)
-#pragma unroll
-        for (int d = 0; d < VN; ++d) acc[h][d] *= al[h];
-    }
-#pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      if (!vok[i]) continue;
-      const float4 plo = *reinterpret_cast<const float4 *>(&p_s[g][i][0]);
-      const float4 phi = *reinterpret_cast<const float4 *>(&p_s[g][i][4]);
-      const float pv[8] = {plo.x, plo.y, plo.z, plo.w, phi.x, phi.y, phi.z, phi.w};
-      float vf[VN];
-      V::unpack(vv[i], vf);
-#pragma unroll
-      for (int h = 0; h < 8; ++h)
-#pragma unroll
-        for (int d = 0; d < VN; ++d) acc[h][d] = fmaf(pv[h], vf[d], acc[h][d]);
-    }
-    __syncwarp();
   }
-
-  // partial state of heads g*G .. g*G+G-1 for split s
-  const size_t rh0 = static_cast<size_t>(r) * Hq + static_cast<size_t>(g) * G;
-  if (g4 == 0) {
-    const int h0 = 2 * c4, h1 = 2 * c4 + 1;
-    if (h0 < G) {
-      p.part_m[(rh0 + h0) * S + s] = m0 == -INFINITY ? -INFINITY : m0 * kLn2;
-      p.part_l[(rh0 + h0) * S + s] = l0;
-    }
-    if (h1 < G) {
-      p.part_m[(rh0 + h1) * S + s] = m1 == -INFINITY ? -INFINITY : m1 * kLn2;
-      p.part_l[(rh0 + h1) * S + s] = l1;
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    if (h < G) {
-      float *dst = p.part_acc + ((rh0 + h) * S + s) * D + lane * VN;
-      if constexpr (VN == 4) {
-        *reinterpret_cast<float4 *>(dst) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-      } else {
-        *reinterpret_cast<float2 *>(dst) = make_float2(acc[h][0], acc[h][1]);
-      }
-    }
-  }
+  __syncthreads();
 }
 
 template <int D>
@@ -282,11 +339,47 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
 }  // namespace
 
 cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cudaStream_t st) {
-  const dim3 grid(cfg.num_splits, cfg.max_rows);
-  const int threads = 32 * cfg.num_kv_heads;
-  if (cfg.head_dim == 128) sparse_attn_kernel<128><<<grid, threads, 0, st>>>(p);
-  else if (cfg.head_dim == 64) sparse_attn_kernel<64><<<grid, threads, 0, st>>>(p);
-  else return cudaErrorInvalidValue;
+  AttnLayout lay;
+  lay.row_bytes = cfg.num_kv_heads * cfg.head_dim * 2;
+  lay.row_pitch = lay.row_bytes + 16;
+  const int stage_bytes = 2 * kTokA * lay.row_pitch;
+  int stages = (100 * 1024) / stage_bytes;  // about 100 KB of ring: two CTAs per SM
+  stages = stages < 2 ? 2 : (stages > kMaxStagesA ? kMaxStagesA : stages);
+  lay.stages = stages;
+  uint32_t off = static_cast<uint32_t>(stages) * stage_bytes;
+  lay.off_ok = off;
+  off += stages * kTokA * 4;
+  lay.off_p = off;
+  off += cfg.num_kv_heads * kTokA * 8 * 4;
+  lay.off_a = off;
+  off += cfg.num_kv_heads * 8 * 4;
+  off = (off + 15u) & ~15u;
+  lay.off_bar = off;
+  off += 2 * stages * 8;
+  lay.off_misc = off;
+  off += 16;
+  const size_t smem = off;
+  const int threads = 32 * (1 + cfg.num_kv_heads);
+  cudaError_t e;
+  int per_sm = 0, dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int items = cfg.max_rows * cfg.num_splits;
+  if (cfg.head_dim == 128) {
+    auto k = sparse_attn_kernel<128>;
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem)) != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(items, std::max(1, per_sm) * sms));
+    k<<<grid, threads, smem, st>>>(p, lay);
+  } else if (cfg.head_dim == 64) {
+    auto k = sparse_attn_kernel<64>;
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem)) != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(items, std::max(1, per_sm) * sms));
+    k<<<grid, threads, smem, st>>>(p, lay);
+  } else {
+    return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

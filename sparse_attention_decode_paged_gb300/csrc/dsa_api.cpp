@@ -93,7 +93,7 @@ dsa_status_t dsa_validate_config(const dsa_config_t *c) {
   if (c->num_q_heads / c->num_kv_heads > 8)
     return fail(DSA_ERR_UNSUPPORTED, "more than 8 query heads per KV head (%d)",
                 c->num_q_heads / c->num_kv_heads);
-  if (c->num_kv_heads > 16) return fail(DSA_ERR_UNSUPPORTED, "num_kv_heads %d > 16", c->num_kv_heads);
+  if (c->num_kv_heads > 8) return fail(DSA_ERR_UNSUPPORTED, "num_kv_heads %d > 8", c->num_kv_heads);
   if (!is_one_of(c->head_dim, {64, 128}))
     return fail(DSA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", c->head_dim);
   if (c->idx_heads < 1 || c->idx_heads > 64)
@@ -303,6 +303,7 @@ dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void 
   p.num_kv_heads = cfg->num_kv_heads;
   p.topk = cfg->topk;
   p.num_splits = cfg->num_splits;
+  p.max_rows_attn = cfg->max_rows;
   p.max_reqs = cfg->max_reqs;
   p.max_pages_per_req = cfg->max_pages_per_req;
   p.score_width = cfg->score_width;

@@ -45,7 +45,7 @@ struct AttnParams {
   float *part_acc;         // [R, Hq, S, D]
   uint32_t *status;
   int32_t num_q_heads, num_kv_heads, topk, num_splits;
-  int32_t max_reqs, max_pages_per_req, score_width, num_pages, page_size;
+  int32_t max_rows_attn, max_reqs, max_pages_per_req, score_width, num_pages, page_size;
   float sm_scale_log2;     // sm_scale * log2(e)
 };
 

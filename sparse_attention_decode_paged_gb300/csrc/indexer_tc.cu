@@ -16,16 +16,21 @@
 //  * Warp 0 (producer): lane 0 streams each tile's pages with 2-D TMA loads
 //    (one box per page and 128-byte K atom, 128-byte swizzle) into a ring of
 //    shared-memory stages; when the score block changes, the whole warp
-//    stages the block's queries as the MMA's B operand (swizzled by hand; fp8
-//    keys: each query head is quantised to e4m3 with scale amax/448 and the
-//    scale is folded into the head weight, ReLU(s x) = s ReLU(x) for s > 0).
+//    stages the block's queries as the MMA's B operand (swizzled by hand).
+//    fp8 keys: each query head x is written as two e4m3 terms with one scale
+//    s = amax/448, x/s = hi + lo (lo = the e4m3 rounding of the residual),
+//    and both terms are multiplied by the same key tile into the same
+//    accumulator (relative error about 2^-8); s is folded into the head
+//    weight since ReLU(s y) = s ReLU(y) for s > 0.
 //  * Warp 1 (MMA): one thread issues tcgen05.mma, transposed so that the key
 //    tile is A (M = 128 tokens) and the block's queries are B (N = 16..256
 //    heads x rows), accumulating in fp32 in tensor memory; two accumulator
 //    buffers let the epilogue of tile i overlap the MMAs of tile i+1.
-//  * Warps 2..5 (epilogue): thread i owns TMEM lane i = token i of the tile,
-//    reads its heads with tcgen05.ld, forms sum_h w_h ReLU(acc_h) with no
-//    cross-thread reduction, scales by s_t and stores the score.
+//  * Warps 2..9 (epilogue, two warpgroups, one per accumulator buffer so
+//    each has two tiles' time): thread i of a warpgroup owns TMEM lane i =
+//    token i of the tile, reads its heads with tcgen05.ld, forms
+//    sum_h w_h ReLU(acc_h) with no cross-thread reduction, scales by s_t and
+//    stores the score.
 //  * Every wait is bounded; a wait that runs out sets DSA_DEV_TIMEOUT and an
 //    abort flag that releases the other roles, the producer waits for its
 //    copies in flight and the MMA warp for its MMAs, and TMEM is freed.
@@ -40,7 +45,7 @@ namespace dsa {
 namespace {
 
 constexpr int kTok = 128;  // tokens per key tile (MMA M)
-constexpr int kWarps = 6;  // 0 producer, 1 MMA, 2..5 epilogue
+constexpr int kWarps = 10;  // 0 producer, 1 MMA, 2..5 and 6..9 two epilogue warpgroups
 constexpr int kThreads = kWarps * 32;
 constexpr long long kWaitBudget = 2000000000LL;  // SM cycles (about 1 s)
 constexpr int kMaxRowsTc = 4096;                  // prefix table capacity
@@ -134,7 +139,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sb = smem_raw + (base - raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = lay.stages, NQ = lay.nq, HP = lay.hp, NMAX = lay.n_max;
-  const uint32_t qbufB = static_cast<uint32_t>(NMAX) * RB * ATOMS;
+  constexpr int kParts = F8 ? 2 : 1;              // fp8: hi and lo query terms
+  const uint32_t qpartB = static_cast<uint32_t>(NMAX) * RB * ATOMS;
+  const uint32_t qbufB = qpartB * kParts;
   const uint32_t stage0 = base;
   const uint32_t q0 = base + lay.off_q;
   float *wbuf = reinterpret_cast<float *>(sb + lay.off_w);            // [NQ][NMAX]
@@ -214,9 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < 2; ++q) {
       tc::mbar_init(QFULL(q), 1);
-      tc::mbar_init(QEMPTY(q), 1 + 4);  // MMA commit + 4 epilogue warps
+      tc::mbar_init(QEMPTY(q), 1 + 8);  // MMA commit + 8 epilogue warps
       tc::mbar_init(TFULL(q), 1);
-      tc::mbar_init(TEMPTY(q), 4);
+      tc::mbar_init(TEMPTY(q), 4);      // the 4 warps of the owning warpgroup
     }
     tc::mbar_init(DONE, 1);
     tc::fence_mbar_init();
@@ -274,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = 1.f / sigma;
             for (int a = 0; a < ATOMS; ++a)
               for (int c = 0; c < RB / 16; ++c) {  // 16 e4m3 per chunk
-                uint32_t o[4] = {0u, 0u, 0u, 0u};
+                uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
                 const int d0 = a * RB + c * 16;
                 if (live && d0 < DIr) {
                   const uint4 v0 = *reinterpret_cast<const uint4 *>(src + d0 * 2);
@@ -282,13 +289,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint32_t w8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
                   for (int k = 0; k < 8; ++k) {
-                    const __nv_fp8x2_storage_t pr = __nv_cvt_float2_to_fp8x2(
-                        make_float2(bf16lo(w8[k]) * inv, bf16hi(w8[k]) * inv), __NV_SATFINITE, __NV_E4M3);
-                    o[k >> 1] |= static_cast<uint32_t>(pr) << (16 * (k & 1));
+                    const float x0 = bf16lo(w8[k]) * inv, x1 = bf16hi(w8[k]) * inv;
+                    const __nv_fp8x2_storage_t ph =
+                        __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+                    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(ph, __NV_E4M3);
+                    const float2 hf = __half22float2(*reinterpret_cast<__half2 *>(&hr));
+                    const __nv_fp8x2_storage_t pl = __nv_cvt_float2_to_fp8x2(
+                        make_float2(x0 - hf.x, x1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+                    hi[k >> 1] |= static_cast<uint32_t>(ph) << (16 * (k & 1));
+                    lo[k >> 1] |= static_cast<uint32_t>(pl) << (16 * (k & 1));
                   }
                 }
-                *reinterpret_cast<uint4 *>(qdst + a * NMAX * RB + swizzle<RB>(n * RB + c * 16)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
+                const uint32_t o = a * NMAX * RB + swizzle<RB>(n * RB + c * 16);
+                *reinterpret_cast<uint4 *>(qdst + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(qdst + qpartB + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
               }
           } else {
             for (int a = 0; a < ATOMS; ++a)
@@ -374,8 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kKsteps; ++k) {
             const uint64_t ad = make_desc<RB>(stage0 + s * kStageB + a * kAtomB + k * 32);
-            const uint64_t bd = make_desc<RB>(q0 + qb * qbufB + a * NMAX * RB + k * 32);
-            tc::mma<F8>(d, ad, bd, idesc, (a | k) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int part = 0; part < kParts; ++part) {
+              const uint64_t bd = make_desc<RB>(q0 + qb * qbufB + part * qpartB + a * NMAX * RB + k * 32);
+              tc::mma<F8>(d, ad, bd, idesc, (a | k | part) != 0 ? 1u : 0u);
+            }
           }
         tc::mma_commit(EMPTY(s));
         tc::mma_commit(TFULL(ab));
@@ -394,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ======================================================= epilogue
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int wg = (warp - 2) >> 2;  // warpgroup: owns accumulator buffer wg
+    const int quarter = warp & 3;    // TMEM lanes 32*quarter .. +31
     const int tl = quarter * 32 + lane;
     int cur = -1, qcount = -1, qb = 0;
     BlockInfo bi{};
@@ -414,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
+      if (ab != wg) continue;  // the other warpgroup's tile
       if (!warp_wait(TFULL(ab), (it >> 1) & 1, abort_flag)) {
         if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
         break;
@@ -433,11 +452,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(ab * NMAX);
       for (int rr = 0; rr < bi.nrows; ++rr) {
         float sum = 0.f;
-        for (int c = 0; c < HP; c += 16) {
-          float v[16];
-          tc::tmem_ld16_sync(trow + rr * HP + c, v);
+        if (HP == 64) {
+          float v[64];
+          tc::tmem_ld64_sync(trow + rr * 64, v);
+          const float4 *w4 = reinterpret_cast<const float4 *>(wq + rr * 64);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sum = fmaf(wq[rr * HP + c + i], fmaxf(v[i], 0.f), sum);
+          for (int i = 0; i < 16; ++i) {
+            const float4 ww = w4[i];
+            sum = fmaf(ww.x, fmaxf(v[4 * i], 0.f), sum);
+            sum = fmaf(ww.y, fmaxf(v[4 * i + 1], 0.f), sum);
+            sum = fmaf(ww.z, fmaxf(v[4 * i + 2], 0.f), sum);
+            sum = fmaf(ww.w, fmaxf(v[4 * i + 3], 0.f), sum);
+          }
+        } else {
+          for (int c = 0; c < HP; c += 16) {
+            float v[16];
+            tc::tmem_ld16_sync(trow + rr * HP + c, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sum = fmaf(wq[rr * HP + c + i], fmaxf(v[i], 0.f), sum);
+          }
         }
         int L = bi.lens[0];
 #pragma unroll
@@ -496,7 +529,7 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
   while (cols < 2 * lay.n_max) cols <<= 1;
   lay.tmem_cols = cols;
   const uint32_t stageB = kTok * RB * ATOMS;
-  const uint32_t qbufB = static_cast<uint32_t>(lay.n_max) * RB * ATOMS;
+  const uint32_t qbufB = static_cast<uint32_t>(lay.n_max) * RB * ATOMS * (F8 ? 2 : 1);
   auto fixed = [&](int nq) {
     uint32_t off = nq * qbufB;                    // query buffers (after the stages)
     off += nq * lay.n_max * 4;                    // weights
