@@ -377,6 +377,11 @@ def run_dsa(args):
             flush.fill_(k & 0xFF)
             graph.replay()
         stream.synchronize()
+        status = dsa.dsa_read_device_status(dev.workspace, stream)
+        if status:  # a device-side check fired: report it instead of timing a broken step
+            sampler.stop()
+            print(json.dumps({"metric": METRIC, "error": f"device status 0x{status:x} after warm-up"}), flush=True)
+            sys.exit(1)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()

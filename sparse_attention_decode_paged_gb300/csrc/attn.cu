@@ -91,7 +91,7 @@ __device__ __forceinline__ bool warp_wait_a(uint32_t bar, uint32_t parity, const
 }
 
 template <int D>
-__global__ void __launch_bounds__(32 * (1 + kMaxKvHeads)) sparse_attn_kernel(const AttnParams p,
+__global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(const AttnParams p,
                                                                               const AttnLayout lay) {
   using V = VecV<D>;
   constexpr int VN = V::kN;  // value dims per lane
@@ -131,41 +131,44 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads)) sparse_attn_kernel(con
       const RowSplit x = row_split(p, item, lane == 0);
       const int32_t *sel = p.topk_idx + static_cast<size_t>(x.r) * p.topk;
       const int32_t *pt = p.page_table + static_cast<size_t>(x.req) * p.max_pages_per_req;
-      for (int base = x.a; base < x.b; base += kTokA, ++chunk) {
-        const int st = chunk % NST;
-        if (!warp_wait_a(EMPTY(st), ((chunk / NST) & 1) ^ 1, abort_flag)) {
-          if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
-          stop = true;
-          break;
-        }
+      // resolve 32 slots per round (one L2 round trip for the indices and
+      // one for the page ids), then issue them as 4 stages of 8 tokens
+      for (int base = x.a; base < x.b && !stop; base += 4 * kTokA) {
         long long off = -1;  // element offset of the token row
-        if (lane < kTokA) {
-          const int i = base + lane;
-          if (i < x.b) {
-            const int t = sel[i];
-            if (t != -1) {
-              if (t < 0 || t >= x.L) {
-                flag_status(p.status, DSA_DEV_BAD_INDEX);
-              } else {
-                const int page = pt[t / p.page_size];
-                if (page < 0 || page >= p.num_pages)
-                  flag_status(p.status, DSA_DEV_BAD_PAGE);
-                else
-                  off = (static_cast<long long>(page) * p.page_size + (t % p.page_size)) * tok_stride;
-              }
+        const int i = base + lane;
+        if (i < x.b) {
+          const int t = sel[i];
+          if (t != -1) {
+            if (t < 0 || t >= x.L) {
+              flag_status(p.status, DSA_DEV_BAD_INDEX);
+            } else {
+              const int page = pt[t / p.page_size];
+              if (page < 0 || page >= p.num_pages)
+                flag_status(p.status, DSA_DEV_BAD_PAGE);
+              else
+                off = (static_cast<long long>(page) * p.page_size + (t % p.page_size)) * tok_stride;
             }
           }
-          tok_ok[st * kTokA + lane] = off >= 0 ? 1 : 0;
         }
-        const uint32_t valid = __ballot_sync(0xFFFFFFFFu, off >= 0);
-        __syncwarp();
-        if (lane == 0)
-          tc::mbar_arrive_expect_tx(FULL(st), static_cast<uint32_t>(__popc(valid)) * 2u * lay.row_bytes);
-        __syncwarp();
-        if (off >= 0) {
-          const uint32_t dk = sbase + st * stageB + lane * pitch;
-          tc::bulk_load(dk, p.k_cache + off * 2, lay.row_bytes, FULL(st), policy);
-          tc::bulk_load(dk + kTokA * pitch, p.v_cache + off * 2, lay.row_bytes, FULL(st), policy);
+        for (int sub = 0; sub < 4 && base + sub * kTokA < x.b; ++sub, ++chunk) {
+          const int st = chunk % NST;
+          if (!warp_wait_a(EMPTY(st), ((chunk / NST) & 1) ^ 1, abort_flag)) {
+            if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+            stop = true;
+            break;
+          }
+          const bool mine = (lane >> 3) == sub;
+          if (mine) tok_ok[st * kTokA + (lane & 7)] = off >= 0 ? 1 : 0;
+          const uint32_t valid = __ballot_sync(0xFFFFFFFFu, mine && off >= 0);
+          __syncwarp();
+          if (lane == 0)
+            tc::mbar_arrive_expect_tx(FULL(st), static_cast<uint32_t>(__popc(valid)) * 2u * lay.row_bytes);
+          __syncwarp();
+          if (mine && off >= 0) {
+            const uint32_t dk = sbase + st * stageB + (lane & 7) * pitch;
+            tc::bulk_load(dk, p.k_cache + off * 2, lay.row_bytes, FULL(st), policy);
+            tc::bulk_load(dk + kTokA * pitch, p.v_cache + off * 2, lay.row_bytes, FULL(st), policy);
+          }
         }
       }
     }

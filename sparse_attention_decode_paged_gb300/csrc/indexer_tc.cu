@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================================================== producer
     const uint64_t policy = tc::l2_evict_first_policy();
     int cur = -1, qcount = -1, issued = 0;
+    int win_base = 0, win_page = -1;  // page ids win_base + lane, held by lane
     BlockInfo bi{};
     const int32_t *pt = nullptr;
     for (; wk.valid(); wk.next()) {
@@ -253,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++qcount;
         bi = load_block(p, cur);
         pt = p.page_table + static_cast<size_t>(bi.req) * p.max_pages_per_req;
+        win_base = -64;  // force a window load for the new block
         const int qb = qcount % NQ;
         if (!warp_wait(QEMPTY(qb), ((qcount / NQ) & 1) ^ 1, abort_flag)) {
           if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
@@ -319,31 +321,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(QFULL(qb));
       }
-      if (lane == 0) {
+      {
         const int it = wk.item - beg;
         const int s = it % S;
-        if (!tc::mbar_wait(EMPTY(s), ((it / S) & 1) ^ 1, abort_flag, kWaitBudget)) {
-          *abort_flag = 1;
-          flag_status(p.status, DSA_DEV_TIMEOUT);
-        } else {
-          const int t0 = wk.tile() * kTok;
-          const int P = p.page_size;
-          const int npg = kTok / P;
-          int pages[8];
-          int nvalid = 0;
-          for (int k = 0; k < npg; ++k) {
-            const int t = t0 + k * P;
-            pages[k] = -1;
-            if (t < bi.lmax) {
-              const int pg = pt[t / P];
+        if (!warp_wait(EMPTY(s), ((it / S) & 1) ^ 1, abort_flag)) {
+          if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+          break;
+        }
+        // page ids of this tile from a 32-entry window the whole warp loads
+        // at once (one L2 round trip per 32 pages instead of one per page)
+        const int P = p.page_size;
+        const int npg = kTok / P;
+        const int np_blk = (bi.lmax + P - 1) / P;
+        int pages[8];
+        int nvalid = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          pages[k] = -1;
+          if (k < npg) {
+            const int pi = wk.tile() * npg + k;
+            if (pi >= win_base + 32 || pi < win_base) {
+              win_base = pi;
+              win_page = win_base + lane < np_blk ? pt[win_base + lane] : -1;
+            }
+            const int pg = __shfl_sync(0xFFFFFFFFu, win_page, pi - win_base);
+            if (pi < np_blk) {
               if (pg >= 0 && pg < p.num_pages) {
                 pages[k] = pg;
                 ++nvalid;
-              } else {
+              } else if (lane == 0) {
                 flag_status(p.status, DSA_DEV_BAD_PAGE);
               }
             }
           }
+        }
+        if (lane == 0) {
           tc::mbar_arrive_expect_tx(FULL(s), static_cast<uint32_t>(nvalid) * P * RB * ATOMS);
           for (int k = 0; k < npg; ++k) {
             if (pages[k] < 0) continue;
@@ -352,11 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::tma_load_2d(stage0 + s * kStageB + a * kAtomB + k * P * RB, &kmap, a * (RB / kElem),
                               pages[k] * P, FULL(s), policy);
           }
-          ++issued;
         }
+        ++issued;
       }
       __syncwarp();
-      if (__shfl_sync(0xFFFFFFFFu, *abort_flag, 0)) break;
     }
     // no copy may land after the CTA exits: wait for the last stages issued
     if (lane == 0)
