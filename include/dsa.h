@@ -249,6 +249,32 @@ dsa_status_t dsa_merge(const dsa_config_t *cfg, const float *part_m, const float
 dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *args, void *workspace,
                       dsa_stream_t stream);
 
+/*
+ * dsa_step_noalloc -- dsa_step for callers that cannot allocate device
+ * memory: code running inside CUDA-graph stream capture (cudaMalloc cannot
+ * be captured), runtimes whose device memory is owned by another allocator,
+ * and C hosts without a device allocator.  The page has no counterpart for
+ * this entry point; it exists for those callers.
+ *
+ * The step's intermediates (status word, scores, top-k, split partials) go
+ * to a 32 MiB array inside the library's device image instead of a caller
+ * workspace; every GPU that loads the library holds those 32 MiB until the
+ * process exits.  Configs whose dsa_workspace_size exceeds 32 MiB are
+ * rejected with DSA_ERR_CAPACITY before anything is launched.  The call
+ * itself allocates nothing: the first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current, so make
+ * that first call outside stream capture.  All calls on a device share the
+ * array and it keeps the last call's contents; the status word is cleared at
+ * the start of every call.  Calls whose executions overlap on the GPU (other
+ * streams, concurrent graph replays) race on the array.
+ *
+ * args: as dsa_step.  status_out: device uint32 (nullable, 4-byte aligned);
+ * when given, the step's device status word is copied there at the end of
+ * the step, on `stream`.
+ */
+dsa_status_t dsa_step_noalloc(const dsa_config_t *cfg, const dsa_step_args_t *args,
+                              uint32_t *status_out, dsa_stream_t stream);
+
 /* Text of the last error on the calling thread ("" if none). */
 const char *dsa_last_error(void);
 

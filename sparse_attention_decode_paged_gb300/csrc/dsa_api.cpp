@@ -83,6 +83,18 @@ uint32_t *status_word(void *workspace) { return static_cast<uint32_t *>(workspac
 
 }  // namespace
 
+namespace dsa {
+dsa_status_t set_error(dsa_status_t st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+}  // namespace dsa
+
 extern "C" {
 
 dsa_status_t dsa_validate_config(const dsa_config_t *c) {

@@ -56,6 +56,9 @@ struct MergeParams {
   int32_t max_rows, num_q_heads, num_splits;
 };
 
+// Records the thread's last-error text (see dsa_last_error) and returns st.
+dsa_status_t set_error(dsa_status_t st, const char *fmt, ...);
+
 // Each launcher returns the launch error (cudaSuccess when queued).
 cudaError_t launch_indexer(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st);
 cudaError_t launch_indexer_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st);

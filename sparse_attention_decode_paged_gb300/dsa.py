@@ -38,7 +38,7 @@ EXPORTED = (
     "dsa_validate_config", "dsa_workspace_size", "dsa_workspace_layout",
     "dsa_reset_device_status", "dsa_read_device_status", "dsa_build_rows",
     "dsa_indexer_scores", "dsa_topk", "dsa_sparse_attn", "dsa_merge", "dsa_step",
-    "dsa_last_error", "dsa_version",
+    "dsa_step_noalloc", "dsa_last_error", "dsa_version",
 )
 
 
@@ -87,6 +87,7 @@ def _load():
         "dsa_sparse_attn": [cfgp] + [vp] * 12,
         "dsa_merge": [cfgp] + [vp] * 6,
         "dsa_step": [cfgp, ctypes.POINTER(dsa_step_args_t), vp, vp],
+        "dsa_step_noalloc": [cfgp, ctypes.POINTER(dsa_step_args_t), vp, vp],
     }
     for name, args in proto.items():
         fn = getattr(lib, name)
@@ -335,3 +336,14 @@ def dsa_step(cfg, args, workspace, stream=None) -> None:
     if isinstance(args, dict):
         args = make_step_args(cfg, args)
     _check(_lib.dsa_step(ctypes.byref(cfg), ctypes.byref(args), _ws(workspace), _stream(stream)))
+
+
+def dsa_step_noalloc(cfg, args, status=None, stream=None) -> None:
+    """dsa_step with the library's built-in scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory).
+    status: optional CUDA int32 tensor of >= 1 element that receives the
+    step's device status word."""
+    if isinstance(args, dict):
+        args = make_step_args(cfg, args)
+    st = _dev(status, "status", (torch.int32,), 1)
+    _check(_lib.dsa_step_noalloc(ctypes.byref(cfg), ctypes.byref(args), st, _stream(stream)))
