@@ -87,7 +87,7 @@ WORKLOADS = [
         block_rows=1, idx_key_dtype=KEY_BF16, kind="decode"),
     _wl("decode_b64_l32768_topk2048", 2, num_q_heads=64, num_kv_heads=8,
         head_dim=128, idx_heads=64, idx_dim=128, page_size=64, topk=2048,
-        num_splits=8, max_rows=64, max_reqs=64, max_pages_per_req=512,
+        num_splits=19, max_rows=64, max_reqs=64, max_pages_per_req=512,
         score_width=32768, block_rows=1, idx_key_dtype=KEY_BF16, kind="decode"),
     _wl("mixed_48dec_512prefill", 3, num_q_heads=64, num_kv_heads=8,
         head_dim=128, idx_heads=64, idx_dim=128, page_size=64, topk=2048,
