@@ -83,7 +83,7 @@ typedef enum { DSA_KEY_BF16 = 0, DSA_KEY_FP8_E4M3 = 1 } dsa_key_dtype_t;
  *   num_kv_heads <= 8, head_dim in {64, 128}, max_rows <= 4096;
  *   1 <= idx_heads <= 64, idx_dim in {32, 64, 128};
  *   page_size in {16, 32, 64, 128}; 1 <= block_rows <= 4;
- *   1 <= topk <= score_width <= max_pages_per_req * page_size;
+ *   1 <= topk <= score_width <= min(262144, max_pages_per_req * page_size);
  *   1 <= num_splits <= 64; sm_scale > 0 and finite.
  */
 typedef struct {

@@ -14,8 +14,11 @@
 // head g: scores on the tensor cores (mma.sync m16n8k16 with the group's <= 8
 // query heads as the A rows and 8 keys as N; key fragments by ldmatrix from
 // rows padded by 16 bytes so the 8 rows hit distinct banks), an online
-// softmax in the log2 domain in fp32, and the value reduction with fp32
-// probabilities and fp32 FMA (each lane owns D/32 value dims of all heads).
+// softmax in the log2 domain in fp32, and the value reduction O^T += V^T P^T
+// on the tensor cores too (mma.sync m16n8k8, V^T by ldmatrix.trans): the
+// score accumulator fragment is already P^T's B fragment, and each fp32
+// probability enters as three bf16 terms hi + mid + lo that sum to it, so
+// the probabilities are not rounded before the value reduction.
 // Bytes in flight are set by the ring depth, not by registers.  Every wait is
 // bounded by an SM-clock budget; a wait that runs out sets DSA_DEV_TIMEOUT.
 //
@@ -35,25 +38,6 @@ constexpr int kMaxKvHeads = 8;  // consumer warps per CTA
 constexpr int kMaxStagesA = 6;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr long long kWaitBudgetA = 2000000000LL;  // SM cycles (about 1 s)
-
-template <int D>
-struct VecV;
-template <>
-struct VecV<128> {
-  using T = uint2;  // 4 bf16
-  static constexpr int kN = 4;
-  __device__ __forceinline__ static void unpack(const T &v, float (&f)[4]) {
-    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-  }
-};
-template <>
-struct VecV<64> {
-  using T = uint32_t;  // 2 bf16
-  static constexpr int kN = 2;
-  __device__ __forceinline__ static void unpack(const T &v, float (&f)[2]) {
-    f[0] = bf16lo(v); f[1] = bf16hi(v);
-  }
-};
 
 struct AttnLayout {
   int stages;
@@ -93,8 +77,6 @@ __device__ __forceinline__ bool warp_wait_a(uint32_t bar, uint32_t parity, const
 template <int D>
 __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(const AttnParams p,
                                                                               const AttnLayout lay) {
-  using V = VecV<D>;
-  constexpr int VN = V::kN;  // value dims per lane
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv, S = p.num_splits;
@@ -102,8 +84,6 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
   const uint32_t sbase = smem_u32(smem);
   const uint32_t stageB = 2u * kTokA * pitch;                      // K block then V block
   int *tok_ok = reinterpret_cast<int *>(smem + lay.off_ok);        // [NST][kTokA]
-  float *p_s = reinterpret_cast<float *>(smem + lay.off_p);        // [Hkv][kTokA][8]
-  float *a_s = reinterpret_cast<float *>(smem + lay.off_a);        // [Hkv][8]
   const uint32_t bar0 = sbase + lay.off_bar;
   auto FULL = [&](int st) { return bar0 + 8u * st; };
   auto EMPTY = [&](int st) { return bar0 + 8u * (NST + st); };
@@ -181,8 +161,6 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     // ============================================ consumers: one per KV head
     const int g = warp - 1;
     const int c4 = lane & 3, g4 = lane >> 2;  // g4: query head of the group (A row)
-    float *pw = p_s + g * kTokA * 8;
-    float *aw = a_s + g * 8;
     int chunk = 0;
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
       const RowSplit x = row_split(p, item, false);
@@ -198,11 +176,10 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
         }
       }
       float m = -INFINITY, l = 0.f;  // head g4, log2 domain
-      float acc[8][VN];
+      // O^T[dim][head] accumulators: o[mt] = dims 16mt + g4 (+8), heads 2c4, 2c4+1
+      float o[D / 16][4];
 #pragma unroll
-      for (int h = 0; h < 8; ++h)
-#pragma unroll
-        for (int d = 0; d < VN; ++d) acc[h][d] = 0.f;
+      for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       bool aborted = false;
       for (int base = x.a; base < x.b; base += kTokA, ++chunk) {
         const int st = chunk % NST;
@@ -213,10 +190,10 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
         }
         const uint32_t kst = sbase + st * stageB;
         const int *ok = tok_ok + st * kTokA;
-        // S[head][token] = Q . K^T over D
+        const int tok = lane & 7, mat = lane >> 3;
+        // S[head][token] = Q . K^T over D (mma m16n8k16: A = query heads, B = keys)
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         {
-          const int tok = lane & 7, mat = lane >> 3;
           const uint32_t kaddr = kst + tok * pitch + (g * D + (mat >> 1) * 16 + (mat & 1) * 8) * 2;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ks += 2) {
@@ -241,32 +218,37 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
         ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
         l = l * al + ps;
         m = mn;
-        pw[(2 * c4) * 8 + g4] = p0;
-        pw[(2 * c4 + 1) * 8 + g4] = p1;
-        if (c4 == 0) aw[g4] = al;
-        __syncwarp();
-        {
-          const float4 alo = *reinterpret_cast<const float4 *>(aw);
-          const float4 ahi = *reinterpret_cast<const float4 *>(aw + 4);
-          const float alv[8] = {alo.x, alo.y, alo.z, alo.w, ahi.x, ahi.y, ahi.z, ahi.w};
+        // rescale the columns of heads 2c4, 2c4+1 (their factors live in lanes 8c4, 8c4+4)
+        const float al_a = __shfl_sync(0xFFFFFFFFu, al, 8 * c4);
+        const float al_b = __shfl_sync(0xFFFFFFFFu, al, 8 * c4 + 4);
 #pragma unroll
-          for (int h = 0; h < 8; ++h)
-#pragma unroll
-            for (int d = 0; d < VN; ++d) acc[h][d] *= alv[h];
+        for (int mt = 0; mt < D / 16; ++mt) {
+          o[mt][0] *= al_a;
+          o[mt][1] *= al_b;
+          o[mt][2] *= al_a;
+          o[mt][3] *= al_b;
         }
-        const uint8_t *vbase = smem + st * stageB + kTokA * pitch + (g * D + lane * VN) * 2;
+        // O^T += V^T . P^T on the tensor cores with the fp32 probabilities kept
+        // exact: p = hi + mid + lo (three bf16 terms), and this lane's (p0, p1)
+        // is already the B fragment (P^T[token 2c4, 2c4+1][head g4]).
+        uint32_t ph, pm, pl;
+        split3_bf16x2(p0, p1, ph, pm, pl);
+        const uint32_t vmask = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
+        const uint32_t vaddr = kst + kTokA * pitch + tok * pitch + (g * D + (mat & 1) * 8 + (mat >> 1) * 16) * 2;
 #pragma unroll
-        for (int j = 0; j < kTokA; ++j) {
-          if (!ok[j]) continue;
-          const float4 plo = *reinterpret_cast<const float4 *>(pw + j * 8);
-          const float4 phi = *reinterpret_cast<const float4 *>(pw + j * 8 + 4);
-          const float pv[8] = {plo.x, plo.y, plo.z, plo.w, phi.x, phi.y, phi.z, phi.w};
-          float vf[VN];
-          V::unpack(*reinterpret_cast<const typename V::T *>(vbase + j * pitch), vf);
-#pragma unroll
-          for (int h = 0; h < 8; ++h)
-#pragma unroll
-            for (int d = 0; d < VN; ++d) acc[h][d] = fmaf(pv[h], vf[d], acc[h][d]);
+        for (int mt = 0; mt < D / 16; mt += 2) {
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4_trans(vaddr + mt * 32, a0, a1, a2, a3);
+          a0 &= vmask;
+          a1 &= vmask;
+          a2 &= vmask;
+          a3 &= vmask;
+          mma_bf16_1688(o[mt], a0, a1, ph);
+          mma_bf16_1688(o[mt], a0, a1, pm);
+          mma_bf16_1688(o[mt], a0, a1, pl);
+          mma_bf16_1688(o[mt + 1], a2, a3, ph);
+          mma_bf16_1688(o[mt + 1], a2, a3, pm);
+          mma_bf16_1688(o[mt + 1], a2, a3, pl);
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(EMPTY(st));
@@ -279,13 +261,14 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
         p.part_l[(rh0 + g4) * S + x.s] = l;
       }
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
+      for (int e = 0; e < 2; ++e) {
+        const int h = 2 * c4 + e;
         if (h < G) {
-          float *dst = p.part_acc + ((rh0 + h) * S + x.s) * D + lane * VN;
-          if constexpr (VN == 4) {
-            *reinterpret_cast<float4 *>(dst) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-          } else {
-            *reinterpret_cast<float2 *>(dst) = make_float2(acc[h][0], acc[h][1]);
+          float *dst = p.part_acc + ((rh0 + h) * S + x.s) * D + g4;
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            dst[16 * mt] = o[mt][e];
+            dst[16 * mt + 8] = o[mt][2 + e];
           }
         }
       }

@@ -36,6 +36,7 @@
 //    copies in flight and the MMA warp for its MMAs, and TMEM is freed.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "dsa_common.cuh"
@@ -127,7 +128,8 @@ struct Walker {
 
 template <int RB, int ATOMS, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
-    indexer_tc_kernel(const IndexerParams p, const TcLayout lay, const __grid_constant__ CUtensorMap kmap) {
+    indexer_tc_kernel(const IndexerParams p, const TcLayout lay, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap qmap) {
   constexpr int kElem = F8 ? 1 : 2;
   constexpr uint32_t kAtomB = kTok * RB;          // one K atom of a key tile
   constexpr uint32_t kStageB = kAtomB * ATOMS;
@@ -228,7 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(DONE, 1);
     tc::fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) tc::tma_prefetch_desc(&kmap);
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&kmap);
+    if constexpr (!F8) tc::tma_prefetch_desc(&qmap);
+  }
   if (warp == 1) {
     tc::tmem_alloc(smem_u32(&misc[0]), static_cast<uint32_t>(lay.tmem_cols));
     tc::tmem_relinquish();
@@ -244,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ======================================================== producer
     const uint64_t policy = tc::l2_evict_first_policy();
+    const uint64_t qpolicy = tc::l2_evict_last_policy();
     int cur = -1, qcount = -1, issued = 0;
     int win_base = 0, win_page = -1;  // page ids win_base + lane, held by lane
     BlockInfo bi{};
@@ -263,63 +269,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stage the block's queries (B operand) and head weights
         uint8_t *qdst = sb + lay.off_q + qb * qbufB;
         float *wdst = wbuf + qb * NMAX;
-        const int DIr = p.idx_dim;  // real dim (<= kDI)
-        for (int n = lane; n < NMAX; n += 32) {
-          const int rr = n / HP, h = n % HP;
-          const bool live = rr < bi.nrows && h < p.idx_heads;
-          const uint8_t *src = p.q_idx + (static_cast<size_t>(bi.first + rr) * p.idx_heads + h) * DIr * 2;
-          float sigma = 1.f;
-          if constexpr (F8) {
-            float amax = 0.f;
-            if (live)
-              for (int d = 0; d < DIr; d += 8) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(src + d * 2);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))),
-                                         fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y)))));
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v.z)), fabsf(bf16hi(v.z))),
-                                         fmaxf(fabsf(bf16lo(v.w)), fabsf(bf16hi(v.w)))));
-              }
-            sigma = amax > 0.f ? amax / 448.f : 1.f;
-            const float inv = 1.f / sigma;
-            for (int a = 0; a < ATOMS; ++a)
-              for (int c = 0; c < RB / 16; ++c) {  // 16 e4m3 per chunk
-                uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
-                const int d0 = a * RB + c * 16;
-                if (live && d0 < DIr) {
-                  const uint4 v0 = *reinterpret_cast<const uint4 *>(src + d0 * 2);
-                  const uint4 v1 = *reinterpret_cast<const uint4 *>(src + d0 * 2 + 16);
-                  const uint32_t w8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-                  for (int k = 0; k < 8; ++k) {
-                    const float x0 = bf16lo(w8[k]) * inv, x1 = bf16hi(w8[k]) * inv;
-                    const __nv_fp8x2_storage_t ph =
-                        __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
-                    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(ph, __NV_E4M3);
-                    const float2 hf = __half22float2(*reinterpret_cast<__half2 *>(&hr));
-                    const __nv_fp8x2_storage_t pl = __nv_cvt_float2_to_fp8x2(
-                        make_float2(x0 - hf.x, x1 - hf.y), __NV_SATFINITE, __NV_E4M3);
-                    hi[k >> 1] |= static_cast<uint32_t>(ph) << (16 * (k & 1));
-                    lo[k >> 1] |= static_cast<uint32_t>(pl) << (16 * (k & 1));
-                  }
-                }
-                const uint32_t o = a * NMAX * RB + swizzle<RB>(n * RB + c * 16);
-                *reinterpret_cast<uint4 *>(qdst + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(qdst + qpartB + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-              }
-          } else {
-            for (int a = 0; a < ATOMS; ++a)
-              for (int c = 0; c < RB / 16; ++c) {  // 8 bf16 per chunk
-                const int d0 = a * (RB / 2) + c * 8;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (live && d0 < DIr) v = *reinterpret_cast<const uint4 *>(src + d0 * 2);
-                *reinterpret_cast<uint4 *>(qdst + a * NMAX * RB + swizzle<RB>(n * RB + c * 16)) = v;
-              }
+        if constexpr (!F8) {
+          // bf16: one TMA box per (row, K atom) writes the swizzled operand
+          // directly; the weights are loaded by the lanes meanwhile
+          for (int n = lane; n < NMAX; n += 32) {
+            const int rr = n / HP, h = n % HP;
+            const bool live = rr < bi.nrows && h < p.idx_heads;
+            wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] : 0.f;
           }
-          wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] * sigma : 0.f;
+          __syncwarp();
+          if (lane == 0) {
+            tc::mbar_arrive_expect_tx(QFULL(qb), static_cast<uint32_t>(bi.nrows) * ATOMS * HP * RB);
+            for (int rr = 0; rr < bi.nrows; ++rr)
+#pragma unroll
+              for (int a = 0; a < ATOMS; ++a)
+                tc::tma_load_2d(q0 + qb * qbufB + a * NMAX * RB + rr * HP * RB, &qmap, a * (RB / kElem),
+                                (bi.first + rr) * p.idx_heads, QFULL(qb), qpolicy);
+          }
+        } else {
+          // fp8: each query head becomes hi + lo e4m3 terms with one scale;
+          // the row's loads are issued together (unrolled) before any math
+          const int DIr = p.idx_dim;
+          for (int n = lane; n < NMAX; n += 32) {
+            const int rr = n / HP, h = n % HP;
+            const bool live = rr < bi.nrows && h < p.idx_heads;
+            const uint8_t *src = p.q_idx + (static_cast<size_t>(bi.first + rr) * p.idx_heads + h) * DIr * 2;
+            float amax = 0.f;
+            uint4 v[RB / 8];  // the whole row: RB e4m3 values = RB bf16 inputs
+#pragma unroll
+            for (int c = 0; c < RB / 8; ++c)
+              v[c] = (live && c * 8 < DIr) ? *reinterpret_cast<const uint4 *>(src + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < RB / 8; ++c) {
+              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v[c].x)), fabsf(bf16hi(v[c].x))),
+                                       fmaxf(fabsf(bf16lo(v[c].y)), fabsf(bf16hi(v[c].y)))));
+              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v[c].z)), fabsf(bf16hi(v[c].z))),
+                                       fmaxf(fabsf(bf16lo(v[c].w)), fabsf(bf16hi(v[c].w)))));
+            }
+            const float sigma = amax > 0.f ? amax / 448.f : 1.f;
+            const float inv = 1.f / sigma;
+#pragma unroll
+            for (int c = 0; c < RB / 16; ++c) {  // 16 e4m3 per 16-byte chunk
+              uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+              const uint32_t w8[8] = {v[2 * c].x, v[2 * c].y, v[2 * c].z, v[2 * c].w,
+                                      v[2 * c + 1].x, v[2 * c + 1].y, v[2 * c + 1].z, v[2 * c + 1].w};
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float x0 = bf16lo(w8[k]) * inv, x1 = bf16hi(w8[k]) * inv;
+                const __nv_fp8x2_storage_t ph =
+                    __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+                __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(ph, __NV_E4M3);
+                const float2 hf = __half22float2(*reinterpret_cast<__half2 *>(&hr));
+                const __nv_fp8x2_storage_t pl =
+                    __nv_cvt_float2_to_fp8x2(make_float2(x0 - hf.x, x1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+                hi[k >> 1] |= static_cast<uint32_t>(ph) << (16 * (k & 1));
+                lo[k >> 1] |= static_cast<uint32_t>(pl) << (16 * (k & 1));
+              }
+              const uint32_t o = swizzle<RB>(n * RB + c * 16);
+              *reinterpret_cast<uint4 *>(qdst + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+              *reinterpret_cast<uint4 *>(qdst + qpartB + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] * sigma : 0.f;
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(QFULL(qb));
         }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(QFULL(qb));
       }
       {
         const int it = wk.item - beg;
@@ -588,12 +603,25 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
+  // queries (bf16 path): rows = (row, head), one box = one row's padded heads
+  CUtensorMap qmap;
+  memset(&qmap, 0, sizeof(qmap));
+  if (!F8) {
+    const cuuint64_t qdim[2] = {static_cast<cuuint64_t>(cfg.idx_dim),
+                                static_cast<cuuint64_t>(cfg.max_rows) * cfg.idx_heads};
+    const cuuint64_t qstride[1] = {static_cast<cuuint64_t>(cfg.idx_dim) * 2};
+    const cuuint32_t qbox[2] = {static_cast<cuuint32_t>(RB / 2), static_cast<cuuint32_t>(lay.hp)};
+    cr = encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t *>(p.q_idx), qdim, qstride, qbox,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<RB, ATOMS, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
   if (grid <= 0) return cudaErrorNoDevice;
-  indexer_tc_kernel<RB, ATOMS, F8><<<grid, kThreads, smem, st>>>(p, lay, kmap);
+  indexer_tc_kernel<RB, ATOMS, F8><<<grid, kThreads, smem, st>>>(p, lay, kmap, qmap);
   return cudaGetLastError();
 }
 
