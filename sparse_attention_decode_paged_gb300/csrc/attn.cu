@@ -39,6 +39,72 @@ constexpr int kMaxStagesA = 6;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr long long kWaitBudgetA = 2000000000LL;  // SM cycles (about 1 s)
 
+// Flash-decoding merge of one (row, head): S partial states -> bf16 output
+// and lse.
+template <int D>
+__device__ __forceinline__ void merge_one(const float *part_m, const float *part_l, const float *part_acc,
+                                          long long rh, int S, uint8_t *out, float *lse, int lane) {
+  constexpr int VN = D / 32;
+  const float *pm = part_m + rh * S, *pl = part_l + rh * S;
+  float ms0 = -INFINITY, ms1 = -INFINITY, ls0 = 0.f, ls1 = 0.f;
+  if (lane < S) { ls0 = __ldcg(pl + lane); ms0 = ls0 > 0.f ? __ldcg(pm + lane) : -INFINITY; }
+  if (lane + 32 < S) { ls1 = __ldcg(pl + lane + 32); ms1 = ls1 > 0.f ? __ldcg(pm + lane + 32) : -INFINITY; }
+  float mx = fmaxf(ms0, ms1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  const float f0 = ms0 == -INFINITY ? 0.f : __expf(ms0 - mx);
+  const float f1 = ms1 == -INFINITY ? 0.f : __expf(ms1 - mx);
+  float lsum = ls0 * f0 + ls1 * f1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+
+  float o[VN];
+#pragma unroll
+  for (int d = 0; d < VN; ++d) o[d] = 0.f;
+  const float *src0 = part_acc + rh * S * D + lane * VN;
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float v[8][VN];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {  // the loads of 8 splits in flight together
+      const int s2 = s0 + u;
+#pragma unroll
+      for (int d = 0; d < VN; ++d) v[u][d] = 0.f;
+      if (s2 < S) {
+        if constexpr (VN == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4 *>(src0 + static_cast<size_t>(s2) * D));
+          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+        } else {
+          const float2 t = __ldcg(reinterpret_cast<const float2 *>(src0 + static_cast<size_t>(s2) * D));
+          v[u][0] = t.x; v[u][1] = t.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int s2 = s0 + u;
+      const float fs = __shfl_sync(0xFFFFFFFFu, (s2 & 32) ? f1 : f0, s2 & 31);
+      if (s2 < S) {
+#pragma unroll
+        for (int d = 0; d < VN; ++d) o[d] = fmaf(fs, v[u][d], o[d]);
+      }
+    }
+  }
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(out) + rh * D + lane * VN;
+#pragma unroll
+  for (int d = 0; d < VN; d += 2)
+    *reinterpret_cast<__nv_bfloat162 *>(dst + d) = __floats2bfloat162_rn(o[d] * inv, o[d + 1] * inv);
+  if (lse && lane == 0) lse[rh] = lsum > 0.f ? mx + logf(lsum) : -INFINITY;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long rh = static_cast<long long>(blockIdx.x) * 8 + warp;  // (row, head)
+  if (rh >= static_cast<long long>(p.max_rows) * p.num_q_heads) return;
+  merge_one<D>(p.part_m, p.part_l, p.part_acc, rh, p.num_splits, p.out, p.lse, lane);
+}
+
 struct AttnLayout {
   int stages;
   int row_bytes;  // Hkv * D * 2: one token's K (or V) row, all KV heads
@@ -275,51 +341,6 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     }
   }
   __syncthreads();
-}
-
-template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
-  constexpr int VN = D / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long rh = static_cast<long long>(blockIdx.x) * 8 + warp;  // (row, head)
-  if (rh >= static_cast<long long>(p.max_rows) * p.num_q_heads) return;
-  const int S = p.num_splits;
-  const float *pm = p.part_m + rh * S, *pl = p.part_l + rh * S;
-  float ms0 = -INFINITY, ms1 = -INFINITY, ls0 = 0.f, ls1 = 0.f;
-  if (lane < S) { ls0 = pl[lane]; ms0 = ls0 > 0.f ? pm[lane] : -INFINITY; }
-  if (lane + 32 < S) { ls1 = pl[lane + 32]; ms1 = ls1 > 0.f ? pm[lane + 32] : -INFINITY; }
-  float mx = fmaxf(ms0, ms1);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-  const float f0 = ms0 == -INFINITY ? 0.f : __expf(ms0 - mx);
-  const float f1 = ms1 == -INFINITY ? 0.f : __expf(ms1 - mx);
-  float lsum = ls0 * f0 + ls1 * f1;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
-
-  float o[VN];
-#pragma unroll
-  for (int d = 0; d < VN; ++d) o[d] = 0.f;
-  for (int s2 = 0; s2 < S; ++s2) {
-    const float fs = __shfl_sync(0xFFFFFFFFu, s2 < 32 ? f0 : f1, s2 & 31);
-    if (fs != 0.f) {
-      const float *src = p.part_acc + (rh * S + s2) * D + lane * VN;
-      if constexpr (VN == 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(src);
-        o[0] = fmaf(fs, v.x, o[0]); o[1] = fmaf(fs, v.y, o[1]);
-        o[2] = fmaf(fs, v.z, o[2]); o[3] = fmaf(fs, v.w, o[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2 *>(src);
-        o[0] = fmaf(fs, v.x, o[0]); o[1] = fmaf(fs, v.y, o[1]);
-      }
-    }
-  }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + rh * D + lane * VN;
-#pragma unroll
-  for (int d = 0; d < VN; d += 2)
-    *reinterpret_cast<__nv_bfloat162 *>(dst + d) = __floats2bfloat162_rn(o[d] * inv, o[d + 1] * inv);
-  if (p.lse && lane == 0) p.lse[rh] = lsum > 0.f ? mx + logf(lsum) : -INFINITY;
 }
 
 }  // namespace

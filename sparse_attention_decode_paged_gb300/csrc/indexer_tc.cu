@@ -7,15 +7,15 @@
 // row only up to its length; commit message 2: the rows of one score block are
 // scored against shared key tiles.
 //
-// Design (one persistent CTA per SM, 6 warps):
+// Design (one persistent CTA per SM, 10 warps):
 //  * Work is the flat list of 128-token key tiles of all score blocks
 //    (block b contributes ceil(L_max(b) / 128) tiles).  Every CTA scans the
 //    block table, prefix-sums the tile counts and takes an equal contiguous
 //    range of tiles, so the launch depends only on the static config while
 //    the work follows the real lengths.
-//  * Warp 0 (producer): lane 0 streams each tile's pages with 2-D TMA loads
-//    (one box per page and 128-byte K atom, 128-byte swizzle) into a ring of
-//    shared-memory stages; when the score block changes, the whole warp
+//  * Warp 0 (producer): streams each tile's pages with 2-D TMA loads (one box
+//    per page and 128-byte K atom, 128-byte swizzle, one lane per box so a
+//    tile's boxes issue in parallel) into a ring of shared-memory stages; when the score block changes, the whole warp
 //    stages the block's queries as the MMA's B operand (swizzled by hand).
 //    fp8 keys: each query head x is written as two e4m3 terms with one scale
 //    s = amax/448, x/s = hi + lo (lo = the e4m3 rounding of the residual),
@@ -370,15 +370,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (lane == 0) {
-          tc::mbar_arrive_expect_tx(FULL(s), static_cast<uint32_t>(nvalid) * P * RB * ATOMS);
-          for (int k = 0; k < npg; ++k) {
-            if (pages[k] < 0) continue;
+        if (lane == 0) tc::mbar_arrive_expect_tx(FULL(s), static_cast<uint32_t>(nvalid) * P * RB * ATOMS);
+        __syncwarp();
+        // one lane per (page, K atom) box: the boxes of a tile are issued in parallel
+        {
+          const int k = lane / ATOMS, a = lane % ATOMS;
+          int pg = -1;
 #pragma unroll
-            for (int a = 0; a < ATOMS; ++a)
-              tc::tma_load_2d(stage0 + s * kStageB + a * kAtomB + k * P * RB, &kmap, a * (RB / kElem),
-                              pages[k] * P, FULL(s), policy);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            if (kk == k) pg = pages[kk];
+          if (lane < npg * ATOMS && pg >= 0)
+            tc::tma_load_2d(stage0 + s * kStageB + a * kAtomB + k * P * RB, &kmap, a * (RB / kElem), pg * P,
+                            FULL(s), policy);
         }
         ++issued;
       }
@@ -482,14 +485,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[64];
           tc::tmem_ld64_sync(trow + rr * 64, v);
           const float4 *w4 = reinterpret_cast<const float4 *>(wq + rr * 64);
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float4 ww = w4[i];
-            sum = fmaf(ww.x, fmaxf(v[4 * i], 0.f), sum);
-            sum = fmaf(ww.y, fmaxf(v[4 * i + 1], 0.f), sum);
-            sum = fmaf(ww.z, fmaxf(v[4 * i + 2], 0.f), sum);
-            sum = fmaf(ww.w, fmaxf(v[4 * i + 3], 0.f), sum);
+            s4[0] = fmaf(ww.x, fmaxf(v[4 * i], 0.f), s4[0]);
+            s4[1] = fmaf(ww.y, fmaxf(v[4 * i + 1], 0.f), s4[1]);
+            s4[2] = fmaf(ww.z, fmaxf(v[4 * i + 2], 0.f), s4[2]);
+            s4[3] = fmaf(ww.w, fmaxf(v[4 * i + 3], 0.f), s4[3]);
           }
+          sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         } else {
           for (int c = 0; c < HP; c += 16) {
             float v[16];
@@ -539,8 +544,8 @@ int sm_count() {
   return n;
 }
 
-constexpr int kSmemLimit = 232448;  // 227 KiB of dynamic shared memory per CTA
-constexpr int kSmemFloor = 120 * 1024;  // keeps one CTA (and one TMEM owner) per SM
+constexpr int kSmemLimit1 = 232448;  // one CTA per SM: 227 KiB of dynamic shared memory
+constexpr int kSmemLimit2 = 113 * 1024;  // two CTAs per SM
 
 template <int RB, int ATOMS, bool F8>
 cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st) {
@@ -554,6 +559,12 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
   int cols = 32;
   while (cols < 2 * lay.n_max) cols <<= 1;
   lay.tmem_cols = cols;
+  // One CTA per SM: the deep key ring (up to 6 stages of 32 KiB) hides the
+  // MMA/epilogue round trip; the floor keeps a second CTA (and a second TMEM
+  // owner) off the SM.
+  const int ctas_per_sm = 1;
+  const int kSmemLimit = ctas_per_sm == 2 ? kSmemLimit2 : kSmemLimit1;
+  const int kSmemFloor = ctas_per_sm == 2 ? 80 * 1024 : 120 * 1024;
   const uint32_t stageB = kTok * RB * ATOMS;
   const uint32_t qbufB = static_cast<uint32_t>(lay.n_max) * RB * ATOMS * (F8 ? 2 : 1);
   auto fixed = [&](int nq) {
@@ -619,7 +630,7 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
   cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<RB, ATOMS, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int grid = sm_count();
+  const int grid = ctas_per_sm * sm_count();
   if (grid <= 0) return cudaErrorNoDevice;
   indexer_tc_kernel<RB, ATOMS, F8><<<grid, kThreads, smem, st>>>(p, lay, kmap, qmap);
   return cudaGetLastError();
