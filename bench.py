@@ -330,6 +330,9 @@ def run_dsa(args):
     inp = W.generate(wl0)
     wl = inp["workload"]
     override = {"num_splits": args.splits} if args.splits else {}
+    # the per-kernel calls below mirror dsa_step, which hands the indexer's
+    # key histogram to the top-k
+    override["flags"] = dsa.DSA_FLAG_TOPK_HISTOGRAM
     dev = DeviceStep(inp, **override)
     cfg, t, v = dev.cfg, dev.t, dev.views
     gen_s = time.time() - t_gen

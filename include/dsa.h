@@ -25,6 +25,8 @@
  *  - bf16 tensors are passed as raw 16-bit storage (const void*); fp8 index
  *    keys as raw OCP E4M3 bytes.  All tensors are dense, row-major, with the
  *    shapes given per argument.
+ *  - The workspace (dsa_workspace_size bytes) must be zero-filled once after
+ *    allocation; the calls keep the parts that must start at zero at zero.
  *  - Every launch size depends only on dsa_config_t.  Lengths, page tables,
  *    row maps and row counts are device data, so changing them between CUDA
  *    graph replays needs no re-capture (commit message 2).  The device calls
@@ -103,7 +105,19 @@ typedef struct {
   int32_t block_rows;        /* G: most rows in one score block                    */
   int32_t idx_key_dtype;     /* dsa_key_dtype_t                                    */
   float sm_scale;            /* softmax scale on q.k                              */
+  int32_t flags;             /* DSA_FLAG_* bits, 0 for none                       */
 } dsa_config_t;
+
+/* Bits of dsa_config_t.flags. */
+enum {
+  /* dsa_indexer_scores also counts, per row, the top 12 bits of each score's
+   * order-preserving key into the workspace histogram, and dsa_topk uses
+   * (then zeroes) those counts instead of recounting.  With this bit set,
+   * every dsa_indexer_scores call must be followed by dsa_topk on the same
+   * scores and workspace before the next dsa_indexer_scores call.  dsa_step
+   * always works this way. */
+  DSA_FLAG_TOPK_HISTOGRAM = 1 << 0
+};
 
 /* Every pointer one fused step needs (all device pointers). */
 typedef struct {
@@ -131,6 +145,7 @@ typedef struct {
   size_t part_m;    /* fp32 [max_rows, num_q_heads, num_splits]           */
   size_t part_l;    /* fp32 [max_rows, num_q_heads, num_splits]           */
   size_t part_acc;  /* fp32 [max_rows, num_q_heads, num_splits, head_dim] */
+  size_t key_hist;  /* uint32 [max_rows, 4096]: score-key histograms (zero between steps) */
   size_t total;     /* bytes to allocate (256-byte aligned regions)       */
 } dsa_workspace_layout_t;
 

@@ -99,6 +99,7 @@ __device__ __forceinline__ void merge_one(const float *part_m, const float *part
 
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+  pdl_wait();  // the partials come from the attention kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long rh = static_cast<long long>(blockIdx.x) * 8 + warp;  // (row, head)
   if (rh >= static_cast<long long>(p.max_rows) * p.num_q_heads) return;
@@ -163,6 +164,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
+  pdl_launch_dependents();
+  pdl_wait();  // the selection comes from the top-k kernel
   __syncthreads();
 
   const int items = p.max_rows_attn * S;
@@ -377,13 +380,13 @@ cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cud
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) != cudaSuccess) return e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem)) != cudaSuccess) return e;
     const int grid = std::max(1, std::min(items, std::max(1, per_sm) * sms));
-    k<<<grid, threads, smem, st>>>(p, lay);
+    if ((e = launch_pdl(k, dim3(grid), dim3(threads), smem, st, 1u, p, lay)) != cudaSuccess) return e;
   } else if (cfg.head_dim == 64) {
     auto k = sparse_attn_kernel<64>;
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) != cudaSuccess) return e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem)) != cudaSuccess) return e;
     const int grid = std::max(1, std::min(items, std::max(1, per_sm) * sms));
-    k<<<grid, threads, smem, st>>>(p, lay);
+    if ((e = launch_pdl(k, dim3(grid), dim3(threads), smem, st, 1u, p, lay)) != cudaSuccess) return e;
   } else {
     return cudaErrorInvalidValue;
   }
@@ -393,9 +396,11 @@ cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cud
 cudaError_t launch_merge(const dsa_config_t &cfg, const MergeParams &p, cudaStream_t st) {
   const long long pairs = static_cast<long long>(cfg.max_rows) * cfg.num_q_heads;
   const unsigned blocks = static_cast<unsigned>((pairs + 7) / 8);
-  if (cfg.head_dim == 128) merge_kernel<128><<<blocks, 256, 0, st>>>(p);
-  else if (cfg.head_dim == 64) merge_kernel<64><<<blocks, 256, 0, st>>>(p);
+  cudaError_t e;
+  if (cfg.head_dim == 128) e = launch_pdl(merge_kernel<128>, dim3(blocks), dim3(256), 0, st, 1u, p);
+  else if (cfg.head_dim == 64) e = launch_pdl(merge_kernel<64>, dim3(blocks), dim3(256), 0, st, 1u, p);
   else return cudaErrorInvalidValue;
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -75,6 +75,8 @@ dsa_status_t layout_of(const dsa_config_t *c, dsa_workspace_layout_t *l) {
   off = align256(off + R * HS * sizeof(float));
   l->part_acc = off;
   off = align256(off + R * HS * c->head_dim * sizeof(float));
+  l->key_hist = off;
+  off = align256(off + R * 4096 * sizeof(uint32_t));
   l->total = off;
   return DSA_OK;
 }
@@ -132,6 +134,8 @@ dsa_status_t dsa_validate_config(const dsa_config_t *c) {
     return fail(DSA_ERR_INVALID_ARG, "idx_key_dtype %d unknown", c->idx_key_dtype);
   if (!(c->sm_scale > 0.f) || !std::isfinite(c->sm_scale))
     return fail(DSA_ERR_INVALID_ARG, "sm_scale must be positive and finite");
+  if ((c->flags & ~static_cast<int32_t>(DSA_FLAG_TOPK_HISTOGRAM)) != 0)
+    return fail(DSA_ERR_INVALID_ARG, "unknown flags 0x%x", c->flags);
   if (static_cast<long long>(c->max_reqs) * c->max_pages_per_req > 0x7FFFFFFFLL)
     return fail(DSA_ERR_INVALID_ARG, "page table larger than 2^31 entries");
   if (c->max_rows > 4096) return fail(DSA_ERR_UNSUPPORTED, "max_rows %d > 4096", c->max_rows);
@@ -225,12 +229,20 @@ dsa_status_t dsa_build_rows(const dsa_config_t *cfg, int32_t num_reqs, const int
   return ok();
 }
 
-dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, const float *w,
-                                const void *idx_cache, const float *idx_scale,
-                                const int32_t *page_table, const int32_t *row_req,
-                                const int32_t *row_len, const int32_t *block_first,
-                                const int32_t *block_nrows, float *scores, void *workspace,
-                                dsa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+uint32_t *key_hist_of(const dsa_config_t *cfg, void *workspace) {
+  dsa_workspace_layout_t l;
+  layout_of(cfg, &l);
+  return reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + l.key_hist);
+}
+
+dsa_status_t indexer_impl(const dsa_config_t *cfg, const void *q_idx, const float *w,
+                          const void *idx_cache, const float *idx_scale, const int32_t *page_table,
+                          const int32_t *row_req, const int32_t *row_len, const int32_t *block_first,
+                          const int32_t *block_nrows, float *scores, void *workspace, bool hist,
+                          dsa_stream_t stream) {
   DSA_CHECK_CFG(cfg);
   DSA_CHECK_DEV_PTR(q_idx);
   DSA_CHECK_DEV_PTR(w);
@@ -264,11 +276,12 @@ dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, cons
   p.num_pages = cfg->num_pages;
   p.page_size = cfg->page_size;
   p.block_rows = cfg->block_rows;
+  p.row_hist = hist ? key_hist_of(cfg, workspace) : nullptr;
   return cuda_status(dsa::launch_indexer_tc(*cfg, p, stream), "indexer launch");
 }
 
-dsa_status_t dsa_topk(const dsa_config_t *cfg, const float *scores, const int32_t *row_len,
-                      int32_t *topk_idx, void *workspace, dsa_stream_t stream) {
+dsa_status_t topk_impl(const dsa_config_t *cfg, const float *scores, const int32_t *row_len,
+                       int32_t *topk_idx, void *workspace, bool hist, dsa_stream_t stream) {
   DSA_CHECK_CFG(cfg);
   DSA_CHECK_DEV_PTR(scores);
   DSA_CHECK_DEV_PTR(row_len);
@@ -279,9 +292,30 @@ dsa_status_t dsa_topk(const dsa_config_t *cfg, const float *scores, const int32_
   p.row_len = row_len;
   p.topk_idx = topk_idx;
   p.status = status_word(workspace);
+  p.row_hist = hist ? key_hist_of(cfg, workspace) : nullptr;
   p.topk = cfg->topk;
   p.score_width = cfg->score_width;
   return cuda_status(dsa::launch_topk(*cfg, p, stream), "top-k launch");
+}
+}  // namespace
+
+extern "C" {
+
+dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, const float *w,
+                                const void *idx_cache, const float *idx_scale,
+                                const int32_t *page_table, const int32_t *row_req,
+                                const int32_t *row_len, const int32_t *block_first,
+                                const int32_t *block_nrows, float *scores, void *workspace,
+                                dsa_stream_t stream) {
+  const bool hist = cfg != nullptr && (cfg->flags & DSA_FLAG_TOPK_HISTOGRAM) != 0;
+  return indexer_impl(cfg, q_idx, w, idx_cache, idx_scale, page_table, row_req, row_len, block_first,
+                      block_nrows, scores, workspace, hist, stream);
+}
+
+dsa_status_t dsa_topk(const dsa_config_t *cfg, const float *scores, const int32_t *row_len,
+                      int32_t *topk_idx, void *workspace, dsa_stream_t stream) {
+  const bool hist = cfg != nullptr && (cfg->flags & DSA_FLAG_TOPK_HISTOGRAM) != 0;
+  return topk_impl(cfg, scores, row_len, topk_idx, workspace, hist, stream);
 }
 
 dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void *k_cache,
@@ -360,11 +394,12 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *a, void *w
   float *part_m = reinterpret_cast<float *>(ws + l.part_m);
   float *part_l = reinterpret_cast<float *>(ws + l.part_l);
   float *part_acc = reinterpret_cast<float *>(ws + l.part_acc);
-  dsa_status_t st = dsa_indexer_scores(cfg, a->q_idx, a->w, a->idx_cache, a->idx_scale,
-                                       a->page_table, a->row_req, a->row_len, a->block_first,
-                                       a->block_nrows, scores, workspace, stream);
+  // the indexer counts the first-level key histogram the top-k then uses
+  dsa_status_t st = indexer_impl(cfg, a->q_idx, a->w, a->idx_cache, a->idx_scale, a->page_table,
+                                 a->row_req, a->row_len, a->block_first, a->block_nrows, scores,
+                                 workspace, true, stream);
   if (st != DSA_OK) return st;
-  st = dsa_topk(cfg, scores, a->row_len, topk_idx, workspace, stream);
+  st = topk_impl(cfg, scores, a->row_len, topk_idx, workspace, true, stream);
   if (st != DSA_OK) return st;
   st = dsa_sparse_attn(cfg, a->q, a->k_cache, a->v_cache, a->page_table, a->row_req, a->row_len,
                        topk_idx, part_m, part_l, part_acc, workspace, stream);

@@ -11,6 +11,27 @@
 
 namespace dsa {
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor is still running; it must
+// wait here before touching the predecessor's output.  Both are no-ops for a
+// kernel launched without that attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Lets the kernel that follows on the stream be scheduled early.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Order-preserving 32-bit key of a score: unsigned order of keys = ranking
+// order of scores (higher first); NaN maps to 0 (below every number, -inf
+// included) and -0 to +0 (so they tie).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0u;
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+constexpr int kKeyBins = 4096;  // first-level histogram: key bits 31..20
+
 // Sticky device status word: set a bit, never clear it.
 __device__ __forceinline__ void flag_status(uint32_t *status, uint32_t bit) {
   if (status) atomicOr(status, bit);

@@ -20,6 +20,7 @@ struct IndexerParams {
   const int32_t *block_nrows;
   float *scores;            // [R, W]
   uint32_t *status;
+  uint32_t *row_hist;       // [R, 4096] key-bin counts for the top-k, or null
   int32_t idx_heads, idx_dim, max_rows, max_reqs, max_pages_per_req, score_width, num_pages;
   int32_t page_size, block_rows;
 };
@@ -29,6 +30,7 @@ struct TopkParams {
   const int32_t *row_len;
   int32_t *topk_idx;
   uint32_t *status;
+  uint32_t *row_hist;  // [R, 4096] filled by the indexer (used, then zeroed), or null
   int32_t topk, score_width;
 };
 
@@ -55,6 +57,34 @@ struct MergeParams {
   float *lse;    // [R, Hq] or null
   int32_t max_rows, num_q_heads, num_splits;
 };
+
+// Launches `kernel` on `st` with programmatic stream serialization, so it may
+// start while the previous kernel on the stream drains (the kernel itself
+// waits with griddepcontrol.wait before reading that kernel's output).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  lc.attrs = attr;
+  lc.numAttrs = n;
+  return cudaLaunchKernelEx(&lc, kernel, args...);
+}
 
 // Records the thread's last-error text (see dsa_last_error) and returns st.
 dsa_status_t set_error(dsa_status_t st, const char *fmt, ...);

@@ -160,6 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int *misc = reinterpret_cast<int *>(sb + lay.off_misc);  // [0] tmem base [1] abort [2..33] scan
   volatile int *abort_flag = misc + 1;
 
+  pdl_launch_dependents();  // the top-k kernel may be scheduled as SMs free up
+
   // ---- tile counts per score block, prefix-summed (every CTA, redundantly)
   const int R = p.max_rows;
   for (int b = tid; b < R; b += kThreads) {
@@ -507,7 +509,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 1; i < 4; ++i)
           if (rr == i) L = bi.lens[i];
-        if (t < L) p.scores[static_cast<size_t>(bi.first + rr) * p.score_width + t] = sum * sc;
+        if (t < L) {
+          const float score = sum * sc;
+          p.scores[static_cast<size_t>(bi.first + rr) * p.score_width + t] = score;
+          if (p.row_hist != nullptr)  // first-level histogram for the top-k that follows
+            atomicAdd(p.row_hist + static_cast<size_t>(bi.first + rr) * kKeyBins + (order_key(score) >> 20), 1u);
+        }
       }
       tc::tc_fence_before();
       __syncwarp();

@@ -72,6 +72,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
+// Arrives on `bar` once every cp.async this thread issued so far has landed
+// (the arrival is counted in the barrier's expected count, .noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ uint64_t l2_evict_last_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));

@@ -13,7 +13,9 @@
 // candidates and counts through distributed shared memory:
 //  A. each CTA loads its segment with 16-byte loads and histograms the top
 //     12 key bits; the cluster sums the histograms and every CTA finds the
-//     bin of the k-th key and how many keys rank above it;
+//     bin of the k-th key and how many keys rank above it (in the fused step
+//     the indexer has already counted the row's bins in the workspace, so
+//     the CTAs read that histogram instead, and zero it for the next step);
 //  B. each CTA counts, per warp, its keys above that bin and copies out the
 //     keys inside it (the candidates, with their positions);
 //  C. every CTA runs the same two 10-bit radix passes over the cluster's
@@ -34,19 +36,12 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins1 = 4096;  // key bits 31..20
+constexpr int kBins1 = kKeyBins;  // key bits 31..20
 constexpr int kBins2 = 1024;  // key bits 19..10, then 9..0
 constexpr int kCandMax = 4096;
 constexpr int kMaxCluster = 8;
 constexpr int kSegPerCta = 16384;  // target keys per CTA
 constexpr int kSegMax = 32768;     // shared-memory capacity per CTA
-
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t b = __float_as_uint(f);
-  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0u;  // NaN: below every number
-  if (b == 0x80000000u) b = 0u;                     // -0 ties with +0
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
 
 struct TopkShared {
   uint32_t hist[kBins1];      // this CTA's histogram (read by the whole cluster)
@@ -118,6 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   TopkShared &sh = *reinterpret_cast<TopkShared *>(smem_raw);
   uint32_t *keys_s = reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(TopkShared) + 15) & ~size_t(15)));
   cg::cluster_group cl = cg::this_cluster();
+  pdl_launch_dependents();
+  pdl_wait();  // the scores come from the indexer kernel
   const int C = static_cast<int>(cl.num_blocks());
   const int q = static_cast<int>(cl.block_rank());
   const int r = blockIdx.x / C;
@@ -129,7 +126,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
     if (tid == 0 && q == 0) flag_status(p.status, DSA_DEV_BAD_ROW);
     L = 0;
   }
+  uint32_t *ghist = p.row_hist != nullptr ? p.row_hist + static_cast<size_t>(r) * kBins1 : nullptr;
   if (L <= K) {  // every position is selected (same branch in every CTA of the cluster)
+    if (ghist != nullptr && q == 0)
+      for (int i = tid; i < kBins1; i += kThreads) ghist[i] = 0u;  // ready for the next step
     const int per = (K + C - 1) / C;
     for (int i = q * per + tid; i < min(K, (q + 1) * per); i += kThreads) out[i] = i < L ? i : -1;
     return;
@@ -164,24 +164,36 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
       if (i4 < n4) {
         const uint4 k = make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
         reinterpret_cast<uint4 *>(keys_s)[i4] = k;
-        atomicAdd(&sh.hist[k.x >> 20], 1u);
-        atomicAdd(&sh.hist[k.y >> 20], 1u);
-        atomicAdd(&sh.hist[k.z >> 20], 1u);
-        atomicAdd(&sh.hist[k.w >> 20], 1u);
+        if (ghist == nullptr) {
+          atomicAdd(&sh.hist[k.x >> 20], 1u);
+          atomicAdd(&sh.hist[k.y >> 20], 1u);
+          atomicAdd(&sh.hist[k.z >> 20], 1u);
+          atomicAdd(&sh.hist[k.w >> 20], 1u);
+        }
       }
     }
   }
   for (int i = n4 * 4 + tid; i < n; i += kThreads) {
     const uint32_t k = order_key(srow[i]);
     keys_s[i] = k;
-    atomicAdd(&sh.hist[k >> 20], 1u);
+    if (ghist == nullptr) atomicAdd(&sh.hist[k >> 20], 1u);
   }
+  // pad the segment to whole 128-key chunks with key 0 (NaN's key): unless the
+  // k-th key lies in bin 0, a 0 is never above, at or inside the threshold bin,
+  // so the hot loops below need no per-key bounds check
+  const int n_pad = (n + 127) & ~127;
+  for (int i = n + tid; i < n_pad; i += kThreads) keys_s[i] = 0u;
   __syncthreads();
-  cl.sync();
-  for (int b = tid; b < kBins1; b += kThreads) {
-    uint32_t s = 0u;
-    for (int rr = 0; rr < C; ++rr) s += cl.map_shared_rank(sh.hist, rr)[b];
-    sh.hist_tot[b] = s;
+  if (ghist != nullptr) {
+    // the indexer already counted the row's key bins
+    for (int b = tid; b < kBins1; b += kThreads) sh.hist_tot[b] = __ldcg(ghist + b);
+  } else {
+    cl.sync();
+    for (int b = tid; b < kBins1; b += kThreads) {
+      uint32_t s = 0u;
+      for (int rr = 0; rr < C; ++rr) s += cl.map_shared_rank(sh.hist, rr)[b];
+      sh.hist_tot[b] = s;
+    }
   }
   __syncthreads();
   uint32_t need = static_cast<uint32_t>(K);
@@ -192,22 +204,22 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   uint32_t prefix = d1 << 20, mask = 0xFFF00000u;
 
   // warp w owns the contiguous 128-key chunks [c_beg, c_end) of the segment
-  const int nchunks = (n + 127) / 128;
+  const int nchunks = n_pad / 128;
   const int per = (nchunks + kWarps - 1) / kWarps;
   const int c_beg = warp * per, c_end = min(nchunks, c_beg + per);
-  const uint32_t lt_mask = (1u << lane) - 1u;
+  const bool checked = d1 == 0;  // the NaN bin is in play: check bounds per key
 
   if (in_bin <= static_cast<uint32_t>(kCandMax)) {
     // ---- B. per-warp count above the bin, candidates inside it
     uint32_t gtw = 0u;
     for (int c = c_beg; c < c_end; ++c) {
       const int i0 = c * 128 + lane * 4;
-      const uint4 kk = i0 < n ? reinterpret_cast<const uint4 *>(keys_s)[i0 >> 2] : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 kk = reinterpret_cast<const uint4 *>(keys_s)[i0 >> 2];
       const uint32_t ks[4] = {kk.x, kk.y, kk.z, kk.w};
       uint32_t hits = 0u;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const bool valid = i0 + j < n;
+        const bool valid = !checked || i0 + j < n;
         const uint32_t top = ks[j] >> 20;
         gtw += (valid && top > d1) ? 1u : 0u;
         hits |= (valid && top == d1) ? (1u << j) : 0u;
@@ -226,15 +238,23 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if (hits & (1u << j)) {
-          sh.cand_key[base] = ks[j];
-          sh.cand_pos[base] = i0 + j;
+          if (base < static_cast<uint32_t>(kCandMax)) {  // holds whenever the histogram is exact
+            sh.cand_key[base] = ks[j];
+            sh.cand_pos[base] = i0 + j;
+          }
           ++base;
         }
     }
     gtw = warp_sum(gtw);
     if (lane == 0) sh.warp_gt[warp] = gtw;
     __syncthreads();
-    cl.sync();  // every CTA's candidates are complete
+    cl.sync();  // every CTA's candidates are complete (and the row histogram was read)
+    if (ghist != nullptr && q == 0)
+      for (int i = tid; i < kBins1; i += kThreads) ghist[i] = 0u;  // ready for the next step
+    if (tid == 0 && sh.count > static_cast<uint32_t>(kCandMax)) {
+      flag_status(p.status, DSA_DEV_BAD_ROW);  // histogram and scores disagree
+      sh.count = kCandMax;
+    }
     // ---- C. the same radix select over the cluster's candidates, in every CTA
 #pragma unroll 1
     for (int shift = 10; shift >= 0; shift -= 10) {
@@ -265,6 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
     }
   } else {
     // heavy ties: two more 10-bit passes over the whole row
+    if (ghist != nullptr) {
+      cl.sync();  // every CTA has read the row histogram
+      if (q == 0)
+        for (int i = tid; i < kBins1; i += kThreads) ghist[i] = 0u;
+    }
 #pragma unroll 1
     for (int shift = 10; shift >= 0; shift -= 10) {
       cl.sync();  // nobody still reads this CTA's previous histogram
@@ -332,12 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   }
   for (int c = c_beg; c < c_end; ++c) {
     const int i0 = c * 128 + lane * 4;
-    const uint4 kk = i0 < n ? reinterpret_cast<const uint4 *>(keys_s)[i0 >> 2] : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 kk = reinterpret_cast<const uint4 *>(keys_s)[i0 >> 2];
     const uint32_t ks[4] = {kk.x, kk.y, kk.z, kk.w};
     uint32_t ng = 0u, ne = 0u;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const bool valid = i0 + j < n;
+      const bool valid = !checked || i0 + j < n;
       ng += (valid && ks[j] > thr) ? 1u : 0u;
       ne += (valid && ks[j] == thr) ? 1u : 0u;
     }
@@ -352,13 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
     uint32_t g = g_before + (excl >> 16), e = e_before + (excl & 0xFFFFu);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const bool valid = i0 + j < n;
+      const bool valid = !checked || i0 + j < n;
       const int t = lo + i0 + j;
       if (valid && ks[j] > thr) {
-        out[g + min(e, need)] = t;
+        const uint32_t pos = g + min(e, need);
+        if (pos < static_cast<uint32_t>(K)) out[pos] = t;
         ++g;
       } else if (valid && ks[j] == thr) {
-        if (e < need) out[g + e] = t;
+        if (e < need && g + e < static_cast<uint32_t>(K)) out[g + e] = t;
         ++e;
       }
     }
@@ -366,7 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
     g_before += tot >> 16;
     e_before += tot & 0xFFFFu;
   }
-  (void)lt_mask;
   cl.sync();  // keep this CTA's shared memory alive until the cluster is done with it
 }
 
@@ -385,19 +410,8 @@ cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, cudaStream
   cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(static_cast<unsigned>(cfg.max_rows * C));
-  lc.blockDim = dim3(kThreads);
-  lc.dynamicSmemBytes = smem;
-  lc.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, topk_cluster_kernel, p);
+  e = launch_pdl(topk_cluster_kernel, dim3(static_cast<unsigned>(cfg.max_rows * C)), dim3(kThreads), smem, st,
+                 static_cast<unsigned>(C), p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -34,6 +34,8 @@ DSA_DEV_TIMEOUT = 1 << 4
 DSA_KEY_BF16 = 0
 DSA_KEY_FP8_E4M3 = 1
 
+DSA_FLAG_TOPK_HISTOGRAM = 1 << 0
+
 EXPORTED = (
     "dsa_validate_config", "dsa_workspace_size", "dsa_workspace_layout",
     "dsa_reset_device_status", "dsa_read_device_status", "dsa_build_rows",
@@ -52,7 +54,8 @@ class dsa_config_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_q_heads", "num_kv_heads", "head_dim", "idx_heads", "idx_dim", "page_size",
         "topk", "num_splits", "max_rows", "max_reqs", "max_pages_per_req", "score_width",
-        "num_pages", "block_rows", "idx_key_dtype")] + [("sm_scale", ctypes.c_float)]
+        "num_pages", "block_rows", "idx_key_dtype")] + [("sm_scale", ctypes.c_float),
+                                                        ("flags", ctypes.c_int32)]
 
 
 class dsa_step_args_t(ctypes.Structure):
@@ -63,7 +66,7 @@ class dsa_step_args_t(ctypes.Structure):
 
 class dsa_workspace_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "status", "scores", "topk_idx", "part_m", "part_l", "part_acc", "total")]
+        "status", "scores", "topk_idx", "part_m", "part_l", "part_acc", "key_hist", "total")]
 
 
 def _load():
@@ -117,12 +120,12 @@ def version() -> str:
 # ----------------------------------------------------------------------------
 def make_config(*, num_q_heads, num_kv_heads, head_dim, idx_heads, idx_dim, page_size, topk,
                 num_splits, max_rows, max_reqs, max_pages_per_req, score_width, num_pages,
-                block_rows=1, idx_key_dtype=DSA_KEY_BF16, sm_scale=None) -> dsa_config_t:
+                block_rows=1, idx_key_dtype=DSA_KEY_BF16, sm_scale=None, flags=0) -> dsa_config_t:
     if sm_scale is None:
         sm_scale = 1.0 / float(np.sqrt(head_dim))
     return dsa_config_t(num_q_heads, num_kv_heads, head_dim, idx_heads, idx_dim, page_size, topk,
                         num_splits, max_rows, max_reqs, max_pages_per_req, score_width,
-                        num_pages, block_rows, idx_key_dtype, float(sm_scale))
+                        num_pages, block_rows, idx_key_dtype, float(sm_scale), int(flags))
 
 
 def config_from_workload(wl, num_pages: int, **override) -> dsa_config_t:

@@ -269,3 +269,33 @@ def test_device_bounds_flags(dsa_lib, cuda_ok):
     dsa_lib.dsa_reset_device_status(dev.workspace)
     dev.step()
     assert dev.status() == 0
+
+
+# ----------------------------------------------------------------------------
+# indexer -> top-k histogram hand-off (DSA_FLAG_TOPK_HISTOGRAM, always on in dsa_step)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("i", [1, 3, 4])
+def test_topk_histogram_handoff(i, dsa_lib, cuda_ok):
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    inp = W.generate(i)
+    plain = DeviceStep(inp)
+    fused = DeviceStep(inp, flags=dsa_lib.DSA_FLAG_TOPK_HISTOGRAM)
+    for dev in (plain, fused):
+        cfg, t, v = dev.cfg, dev.t, dev.views
+        for _ in range(2):  # the second pass needs the histogram re-zeroed by the first top-k
+            dsa_lib.dsa_indexer_scores(cfg, t["q_idx"], t["w"], t["idx_cache"], t["idx_scale"], t["page_table"],
+                                       t["row_req"], t["row_len"], t["block_first"], t["block_nrows"],
+                                       v["scores"], dev.workspace)
+            dsa_lib.dsa_topk(cfg, v["scores"], t["row_len"], v["topk_idx"], dev.workspace)
+        torch.cuda.synchronize()
+        assert dev.status() == 0
+    assert torch.equal(plain.views["scores"], fused.views["scores"])
+    assert torch.equal(plain.views["topk_idx"], fused.views["topk_idx"])
+    hist = dsa_lib.dsa_workspace_layout(fused.cfg)
+    kh = fused.workspace[hist["key_hist"]:hist["total"]]
+    assert int(kh.count_nonzero()) == 0  # left at zero for the next step
+    fused.step()  # dsa_step hands the histogram over internally
+    torch.cuda.synchronize()
+    assert torch.equal(plain.views["topk_idx"], fused.views["topk_idx"])
+    assert int(kh.count_nonzero()) == 0

@@ -58,6 +58,7 @@ def test_validate_config_accepts_all_workloads(dsa_lib):
     (dict(topk=0), 1), (dict(topk=40000), 1), (dict(score_width=40000), 1),
     (dict(num_splits=0), 2), (dict(block_rows=5), 2), (dict(idx_key_dtype=7), 1),
     (dict(sm_scale=-1.0), 1), (dict(sm_scale=float("inf")), 1), (dict(max_rows=0), 1),
+    (dict(flags=6), 1),
 ])
 def test_validate_config_rejects(dsa_lib, bad, status):
     cfg = _cfg(dsa_lib, **bad)
@@ -121,11 +122,12 @@ def test_workspace_layout(dsa_lib):
     cfg = _cfg(dsa_lib)
     lay = dsa_lib.dsa_workspace_layout(cfg)
     assert lay["status"] == 0
-    order = ["status", "scores", "topk_idx", "part_m", "part_l", "part_acc", "total"]
+    order = ["status", "scores", "topk_idx", "part_m", "part_l", "part_acc", "key_hist", "total"]
     offs = [lay[k] for k in order]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lay["topk_idx"] - lay["scores"] >= 64 * 32768 * 4
-    assert lay["total"] - lay["part_acc"] >= 64 * 64 * 8 * 128 * 4
+    assert lay["key_hist"] - lay["part_acc"] >= 64 * 64 * 8 * 128 * 4
+    assert lay["total"] - lay["key_hist"] >= 64 * 4096 * 4
     assert dsa_lib.dsa_workspace_size(cfg) == lay["total"]
 
 
