@@ -26,6 +26,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "dsa_common.cuh"
 #include "tc_ptx.cuh"
@@ -40,15 +41,33 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr long long kWaitBudgetA = 2000000000LL;  // SM cycles (about 1 s)
 
 // Flash-decoding merge of one (row, head): S partial states -> bf16 output
-// and lse.
+// and lse.  Lane j holds dims [j*VN, j*VN + VN) and the states of splits j
+// and j + 32.  The m, l and the first kRound accumulator loads are issued
+// together, so a merge of up to kRound splits costs one memory round trip.
+constexpr int kMergeRound = 24;
+
 template <int D>
 __device__ __forceinline__ void merge_one(const float *part_m, const float *part_l, const float *part_acc,
                                           long long rh, int S, uint8_t *out, float *lse, int lane) {
   constexpr int VN = D / 32;
+  using VecT = typename std::conditional<VN == 4, float4, float2>::type;
   const float *pm = part_m + rh * S, *pl = part_l + rh * S;
-  float ms0 = -INFINITY, ms1 = -INFINITY, ls0 = 0.f, ls1 = 0.f;
-  if (lane < S) { ls0 = __ldcg(pl + lane); ms0 = ls0 > 0.f ? __ldcg(pm + lane) : -INFINITY; }
-  if (lane + 32 < S) { ls1 = __ldcg(pl + lane + 32); ms1 = ls1 > 0.f ? __ldcg(pm + lane + 32) : -INFINITY; }
+  const float *src0 = part_acc + rh * S * D + lane * VN;
+  float ls0 = 0.f, ls1 = 0.f, mr0 = -INFINITY, mr1 = -INFINITY;
+  if (lane < S) { ls0 = __ldcg(pl + lane); mr0 = __ldcg(pm + lane); }
+  if (lane + 32 < S) { ls1 = __ldcg(pl + lane + 32); mr1 = __ldcg(pm + lane + 32); }
+  float v[kMergeRound][VN];
+#pragma unroll
+  for (int u = 0; u < kMergeRound; ++u) {
+    if (u < S) {
+      const VecT t = __ldcg(reinterpret_cast<const VecT *>(src0 + static_cast<size_t>(u) * D));
+      v[u][0] = t.x;
+      v[u][1] = t.y;
+      if constexpr (VN == 4) { v[u][2] = t.z; v[u][3] = t.w; }
+    }
+  }
+  // an empty split (l = 0) carries no weight whatever its m
+  const float ms0 = ls0 > 0.f ? mr0 : -INFINITY, ms1 = ls1 > 0.f ? mr1 : -INFINITY;
   float mx = fmaxf(ms0, ms1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
@@ -61,33 +80,20 @@ __device__ __forceinline__ void merge_one(const float *part_m, const float *part
   float o[VN];
 #pragma unroll
   for (int d = 0; d < VN; ++d) o[d] = 0.f;
-  const float *src0 = part_acc + rh * S * D + lane * VN;
-  for (int s0 = 0; s0 < S; s0 += 8) {
-    float v[8][VN];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {  // the loads of 8 splits in flight together
-      const int s2 = s0 + u;
+  for (int u = 0; u < kMergeRound; ++u) {
+    const float fs = __shfl_sync(0xFFFFFFFFu, f0, u & 31);
+    if (u < S) {
 #pragma unroll
-      for (int d = 0; d < VN; ++d) v[u][d] = 0.f;
-      if (s2 < S) {
-        if constexpr (VN == 4) {
-          const float4 t = __ldcg(reinterpret_cast<const float4 *>(src0 + static_cast<size_t>(s2) * D));
-          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
-        } else {
-          const float2 t = __ldcg(reinterpret_cast<const float2 *>(src0 + static_cast<size_t>(s2) * D));
-          v[u][0] = t.x; v[u][1] = t.y;
-        }
-      }
+      for (int d = 0; d < VN; ++d) o[d] = fmaf(fs, v[u][d], o[d]);
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int s2 = s0 + u;
-      const float fs = __shfl_sync(0xFFFFFFFFu, (s2 & 32) ? f1 : f0, s2 & 31);
-      if (s2 < S) {
-#pragma unroll
-        for (int d = 0; d < VN; ++d) o[d] = fmaf(fs, v[u][d], o[d]);
-      }
-    }
+  }
+  for (int s2 = kMergeRound; s2 < S; ++s2) {  // more splits than one round holds
+    const VecT t = __ldcg(reinterpret_cast<const VecT *>(src0 + static_cast<size_t>(s2) * D));
+    const float fs = __shfl_sync(0xFFFFFFFFu, (s2 & 32) ? f1 : f0, s2 & 31);
+    o[0] = fmaf(fs, t.x, o[0]);
+    o[1] = fmaf(fs, t.y, o[1]);
+    if constexpr (VN == 4) { o[2] = fmaf(fs, t.z, o[2]); o[3] = fmaf(fs, t.w, o[3]); }
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(out) + rh * D + lane * VN;
@@ -325,9 +331,12 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
       if (aborted) break;
       // partial state of heads g*G .. g*G+G-1 for this split
       const size_t rh0 = static_cast<size_t>(x.r) * Hq + static_cast<size_t>(g) * G;
+      // the merge reads them right after this kernel: keep them in L2 while
+      // the K/V stream (evict-first) passes through
+      const uint64_t keep = tc::l2_evict_last_policy();
       if (c4 == 0 && g4 < G) {
-        p.part_m[(rh0 + g4) * S + x.s] = m == -INFINITY ? -INFINITY : m * kLn2;
-        p.part_l[(rh0 + g4) * S + x.s] = l;
+        tc::st_global_hint(p.part_m + (rh0 + g4) * S + x.s, m == -INFINITY ? -INFINITY : m * kLn2, keep);
+        tc::st_global_hint(p.part_l + (rh0 + g4) * S + x.s, l, keep);
       }
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -336,8 +345,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
           float *dst = p.part_acc + ((rh0 + h) * S + x.s) * D + g4;
 #pragma unroll
           for (int mt = 0; mt < D / 16; ++mt) {
-            dst[16 * mt] = o[mt][e];
-            dst[16 * mt + 8] = o[mt][2 + e];
+            tc::st_global_hint(dst + 16 * mt, o[mt][e], keep);
+            tc::st_global_hint(dst + 16 * mt + 8, o[mt][2 + e], keep);
           }
         }
       }

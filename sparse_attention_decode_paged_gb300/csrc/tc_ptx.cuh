@@ -72,11 +72,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
-// Arrives on `bar` once every cp.async this thread issued so far has landed
-// (the arrival is counted in the barrier's expected count, .noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ uint64_t l2_evict_last_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
@@ -86,6 +81,10 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
   return p;
+}
+// fp32 global store with an L2 eviction-priority policy.
+__device__ __forceinline__ void st_global_hint(float *p, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(p), "f"(v), "l"(policy) : "memory");
 }
 // Makes generic-proxy shared-memory writes visible to the async proxy
 // (tensor cores, TMA).
