@@ -73,7 +73,8 @@ enum {
   DSA_DEV_BAD_PAGE = 1u << 1,  /* page-table entry outside [0, num_pages)           */
   DSA_DEV_BAD_INDEX = 1u << 2, /* top-k position outside [0, row_len)               */
   DSA_DEV_BAD_BLOCK = 1u << 3, /* score block outside max_rows or mixing requests   */
-  DSA_DEV_TIMEOUT = 1u << 4    /* a bounded device-side wait ran out                */
+  DSA_DEV_TIMEOUT = 1u << 4,   /* a bounded device-side wait ran out                */
+  DSA_DEV_BAD_HIST = 1u << 5   /* a handed-over key histogram disagrees with scores */
 };
 
 typedef enum { DSA_KEY_BF16 = 0, DSA_KEY_FP8_E4M3 = 1 } dsa_key_dtype_t;
@@ -115,7 +116,12 @@ enum {
    * (then zeroes) those counts instead of recounting.  With this bit set,
    * every dsa_indexer_scores call must be followed by dsa_topk on the same
    * scores and workspace before the next dsa_indexer_scores call.  dsa_step
-   * always works this way. */
+   * always works this way.  dsa_topk checks the hand-over: a row whose
+   * histogram does not count exactly row_len scores (the indexer ran without
+   * the bit, or twice) is recounted from its scores, with the same result; a
+   * histogram with the right total that does not match the scores (the scores
+   * changed in between) sets DSA_DEV_BAD_HIST and that row's selection is
+   * unspecified.  No case reads or writes outside the buffers. */
   DSA_FLAG_TOPK_HISTOGRAM = 1 << 0
 };
 

@@ -55,7 +55,8 @@ struct TopkShared {
 };
 
 // Finds, scanning bins from the top, the bin d with above(d) < need <=
-// above(d) + hist[d]; writes d and above(d) to sh.digit / sh.above.
+// above(d) + hist[d]; writes d and above(d) to sh.digit / sh.above, or nbins
+// and 0 when the histogram holds fewer than `need` keys.
 __device__ __forceinline__ void select_bin(TopkShared &sh, const uint32_t *hist, int nbins, uint32_t need) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = nbins / kThreads;  // 1 or 4 bins per thread, descending
@@ -73,6 +74,10 @@ __device__ __forceinline__ void select_bin(TopkShared &sh, const uint32_t *hist,
     if (lane >= o) incl += v;
   }
   if (lane == 31) sh.scan[warp] = incl;
+  if (tid == 0) {  // no bin: the histogram holds fewer than `need` keys
+    sh.digit = static_cast<uint32_t>(nbins);
+    sh.above = 0u;
+  }
   __syncthreads();
   if (warp == 0) {
     uint32_t v = sh.scan[lane];
@@ -184,10 +189,30 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   const int n_pad = (n + 127) & ~127;
   for (int i = n + tid; i < n_pad; i += kThreads) keys_s[i] = 0u;
   __syncthreads();
-  if (ghist != nullptr) {
-    // the indexer already counted the row's key bins
-    for (int b = tid; b < kBins1; b += kThreads) sh.hist_tot[b] = __ldcg(ghist + b);
-  } else {
+  bool recount = ghist == nullptr;
+  if (!recount) {
+    // the indexer already counted the row's key bins; use them only if they
+    // count exactly the row's L scores (every CTA of the cluster reads the
+    // same counts, so all take the same branch)
+    uint32_t part = 0u;
+    for (int b = tid; b < kBins1; b += kThreads) {
+      const uint32_t v = __ldcg(ghist + b);
+      sh.hist_tot[b] = v;
+      part += v;
+    }
+    part = warp_sum(part);
+    if (lane == 0) sh.scan[warp] = part;
+    __syncthreads();
+    uint32_t total = 0u;
+#pragma unroll 8
+    for (int w = 0; w < kWarps; ++w) total += sh.scan[w];
+    if (total != static_cast<uint32_t>(L)) {
+      recount = true;
+      for (int i = tid; i < n; i += kThreads) atomicAdd(&sh.hist[keys_s[i] >> 20], 1u);
+    }
+  }
+  if (recount) {
+    __syncthreads();
     cl.sync();
     for (int b = tid; b < kBins1; b += kThreads) {
       uint32_t s = 0u;
@@ -198,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   __syncthreads();
   uint32_t need = static_cast<uint32_t>(K);
   select_bin(sh, sh.hist_tot, kBins1, need);
-  const uint32_t d1 = sh.digit;
+  const uint32_t d1 = min(sh.digit, static_cast<uint32_t>(kBins1 - 1));  // found whenever L > K
   need -= sh.above;
   const uint32_t in_bin = sh.hist_tot[d1];
   uint32_t prefix = d1 << 20, mask = 0xFFF00000u;
@@ -256,13 +281,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
       sh.count = kCandMax;
     }
     // ---- C. the same radix select over the cluster's candidates, in every CTA
+    uint32_t cluster_cands = 0u;
 #pragma unroll 1
     for (int shift = 10; shift >= 0; shift -= 10) {
       for (int i = tid; i < kBins2; i += kThreads) sh.hist_tot[i] = 0u;
       __syncthreads();
+      cluster_cands = 0u;
       for (int rr = 0; rr < C; ++rr) {
         const uint32_t *ck = cl.map_shared_rank(sh.cand_key, rr);
-        const uint32_t cnt = *cl.map_shared_rank(&sh.count, rr);
+        const uint32_t cnt = min(*cl.map_shared_rank(&sh.count, rr), static_cast<uint32_t>(kCandMax));
+        cluster_cands += cnt;
         for (uint32_t i = tid; i < cnt; i += kThreads) {
           const uint32_t k = ck[i];
           if ((k & mask) == prefix) atomicAdd(&sh.hist_tot[(k >> shift) & 0x3FFu], 1u);
@@ -270,10 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
       }
       __syncthreads();
       select_bin(sh, sh.hist_tot, kBins2, need);
+      const uint32_t dg = min(sh.digit, static_cast<uint32_t>(kBins2 - 1));  // found if the counts agree
       need -= sh.above;
-      prefix |= sh.digit << shift;
+      prefix |= dg << shift;
       mask |= 0x3FFu << shift;
     }
+    // the candidates the cluster found must be the keys the histogram put in
+    // the k-th key's bin
+    if (tid == 0 && q == 0 && cluster_cands != in_bin) flag_status(p.status, DSA_DEV_BAD_HIST);
     // own candidates above / at the k-th key, credited to the warp that owns them
     const uint32_t thr = prefix;
     const uint32_t cnt = sh.count;
@@ -308,8 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
       }
       __syncthreads();
       select_bin(sh, sh.hist_tot, kBins2, need);
+      const uint32_t dg = min(sh.digit, static_cast<uint32_t>(kBins2 - 1));  // found if the counts agree
+      if (tid == 0 && q == 0 && sh.digit >= static_cast<uint32_t>(kBins2)) flag_status(p.status, DSA_DEV_BAD_HIST);
       need -= sh.above;
-      prefix |= sh.digit << shift;
+      prefix |= dg << shift;
       mask |= 0x3FFu << shift;
     }
     const uint32_t thr = prefix;

@@ -30,6 +30,7 @@ DSA_DEV_BAD_PAGE = 1 << 1
 DSA_DEV_BAD_INDEX = 1 << 2
 DSA_DEV_BAD_BLOCK = 1 << 3
 DSA_DEV_TIMEOUT = 1 << 4
+DSA_DEV_BAD_HIST = 1 << 5
 
 DSA_KEY_BF16 = 0
 DSA_KEY_FP8_E4M3 = 1

@@ -299,3 +299,63 @@ def test_topk_histogram_handoff(i, dsa_lib, cuda_ok):
     torch.cuda.synchronize()
     assert torch.equal(plain.views["topk_idx"], fused.views["topk_idx"])
     assert int(kh.count_nonzero()) == 0
+
+
+def test_topk_histogram_mismatch(dsa_lib, cuda_ok):
+    """A hand-over histogram that does not count the row's scores is recounted
+    (same selection, clean status); one with the right total but the wrong
+    bins sets DSA_DEV_BAD_HIST and stays inside the buffers."""
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    inp = W.generate(1)
+    plain = DeviceStep(inp)
+    plain.step()
+    dev = DeviceStep(inp, flags=dsa_lib.DSA_FLAG_TOPK_HISTOGRAM)
+    cfg, t, v = dev.cfg, dev.t, dev.views
+    cfg_nohist = type(cfg).from_buffer_copy(cfg)
+    cfg_nohist.flags = 0
+    lay = dsa_lib.dsa_workspace_layout(cfg)
+    kh = dev.workspace[lay["key_hist"]:lay["total"]]
+
+    def indexer(c):
+        dsa_lib.dsa_indexer_scores(c, t["q_idx"], t["w"], t["idx_cache"], t["idx_scale"], t["page_table"],
+                                   t["row_req"], t["row_len"], t["block_first"], t["block_nrows"],
+                                   v["scores"], dev.workspace)
+
+    def topk():
+        dsa_lib.dsa_topk(cfg, v["scores"], t["row_len"], v["topk_idx"], dev.workspace)
+
+    # the indexer ran without the bit: nothing counted, the top-k recounts
+    indexer(cfg_nohist)
+    v["topk_idx"].fill_(-7)
+    topk()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    assert torch.equal(v["topk_idx"], plain.views["topk_idx"])
+    # the indexer ran twice with the bit: every bin counted twice, recounted
+    indexer(cfg)
+    indexer(cfg)
+    v["topk_idx"].fill_(-7)
+    topk()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    assert torch.equal(v["topk_idx"], plain.views["topk_idx"])
+    assert int(kh.count_nonzero()) == 0
+    # right total, wrong bins: the scores of one long row change after counting
+    lens = t["row_len"].cpu().numpy()
+    K = cfg.topk
+    r = int(next(i for i, L in enumerate(lens) if L > K))
+    indexer(cfg)
+    v["scores"][r, : int(lens[r])] = -1e30
+    topk()
+    torch.cuda.synchronize()
+    st = dev.status()
+    assert st & dsa_lib.DSA_DEV_BAD_HIST, hex(st)
+    others = [i for i in range(cfg.max_rows) if i != r]
+    assert torch.equal(v["topk_idx"][others], plain.views["topk_idx"][others])
+    assert int(kh.count_nonzero()) == 0
+    dsa_lib.dsa_reset_device_status(dev.workspace)
+    dev.step()  # a clean step afterwards
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    assert torch.equal(v["topk_idx"], plain.views["topk_idx"])
