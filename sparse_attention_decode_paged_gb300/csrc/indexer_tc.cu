@@ -15,8 +15,9 @@
 //    the work follows the real lengths.
 //  * Warp 0 (producer): streams each tile's pages with 2-D TMA loads (one box
 //    per page and 128-byte K atom, 128-byte swizzle, one lane per box so a
-//    tile's boxes issue in parallel) into a ring of shared-memory stages; when the score block changes, the whole warp
-//    stages the block's queries as the MMA's B operand (swizzled by hand).
+//    tile's boxes issue in parallel) into a ring of shared-memory stages;
+//    when the score block changes it stages the block's queries as the
+//    MMA's B operand (bf16 by TMA; fp8 swizzled by hand).
 //    fp8 keys: each query head x is written as two e4m3 terms with one scale
 //    s = amax/448, x/s = hi + lo (lo = the e4m3 rounding of the residual),
 //    and both terms are multiplied by the same key tile into the same
@@ -24,11 +25,13 @@
 //    weight since ReLU(s y) = s ReLU(y) for s > 0.
 //  * Warp 1 (MMA): one thread issues tcgen05.mma, transposed so that the key
 //    tile is A (M = 128 tokens) and the block's queries are B (N = 16..256
-//    heads x rows), accumulating in fp32 in tensor memory; two accumulator
-//    buffers let the epilogue of tile i overlap the MMAs of tile i+1.
-//  * Warps 2..9 (epilogue, two warpgroups, one per accumulator buffer so
-//    each has two tiles' time): thread i of a warpgroup owns TMEM lane i =
-//    token i of the tile, reads its heads with tcgen05.ld, forms
+//    heads x rows), accumulating in fp32 in tensor memory; four accumulator
+//    buffers (two when 4 x N columns do not fit in TMEM) let the epilogue of
+//    tile i overlap the MMAs of the next tiles, so a slow epilogue does not
+//    hold a key stage.
+//  * Warps 2..9 (epilogue, two warpgroups taking alternate tiles, so each
+//    has two tiles' time): thread i of a warpgroup owns TMEM lane i = token
+//    i of the tile, reads its heads with tcgen05.ld, forms
 //    sum_h w_h ReLU(acc_h) with no cross-thread reduction, scales by s_t and
 //    stores the score.
 //  * Every wait is bounded; a wait that runs out sets DSA_DEV_TIMEOUT and an
@@ -56,8 +59,9 @@ struct TcLayout {
   int n_max;      // hp * block_rows: accumulator columns per buffer
   int stages;     // key-tile ring depth
   int nq;         // query buffers (1 or 2)
+  int nacc;       // TMEM accumulator buffers (2 or 4)
   int tmem_cols;  // allocated TMEM columns (power of two >= 32)
-  uint32_t off_q, off_w, off_prefix, off_bar, off_misc;
+  uint32_t off_q, off_w, off_prefix, off_blk, off_bar, off_misc;
 };
 
 template <int RB>
@@ -100,29 +104,71 @@ __device__ __forceinline__ BlockInfo load_block(const IndexerParams &p, int b) {
   return bi;
 }
 
-// Walks this CTA's contiguous range of tiles in order.
+// The score block holding tile `item`: b with pf[b] <= item < pf[b+1].
+__device__ __forceinline__ int find_block(const int *pf, int nblocks, int item) {
+  int lo = 0, hi = nblocks;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pf[mid] <= item) lo = mid;
+    else hi = mid;
+  }
+  while (item >= pf[lo + 1]) ++lo;  // skip blocks without tiles
+  return lo;
+}
+
+// Walks this CTA's contiguous range of tiles in order; the current block's
+// tile range is kept in registers (the loops that use it are latency-bound).
 struct Walker {
   const int *prefix;
-  int item, end, block;
+  int item, end, block, bstart, bnext;
   __device__ __forceinline__ void start(const int *pf, int nblocks, int beg, int e) {
     prefix = pf;
     item = beg;
     end = e;
-    int lo = 0, hi = nblocks;  // find b with pf[b] <= beg < pf[b+1]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (pf[mid] <= beg) lo = mid;
-      else hi = mid;
-    }
-    block = lo;
-    while (item < end && item >= prefix[block + 1]) ++block;
+    block = find_block(pf, nblocks, beg);
+    bstart = pf[block];
+    bnext = pf[block + 1];
   }
   __device__ __forceinline__ bool valid() const { return item < end; }
-  __device__ __forceinline__ int tile() const { return item - prefix[block]; }
-  __device__ __forceinline__ bool last_of_block() const { return item + 1 >= prefix[block + 1] || item + 1 >= end; }
+  __device__ __forceinline__ int tile() const { return item - bstart; }
+  __device__ __forceinline__ bool last_of_block() const { return item + 1 >= bnext || item + 1 >= end; }
   __device__ __forceinline__ void next() {
     ++item;
-    while (item < end && item >= prefix[block + 1]) ++block;
+    if (item < end && item >= bnext) {
+      do {
+        ++block;
+      } while (item >= prefix[block + 1]);
+      bstart = prefix[block];
+      bnext = prefix[block + 1];
+    }
+  }
+};
+
+// The CTA's score blocks, read once into shared memory so that a block change
+// costs no dependent global loads: [kBlkCache][8] = first, nrows, req, lmax,
+// lens[4].  Blocks past the first kBlkCache of the CTA are read from global
+// memory (16 entries cost 512 bytes; more would take a key stage away).
+constexpr int kBlkCache = 16;
+struct BlockCache {
+  const int *tab;
+  int b_lo, n;
+  __device__ __forceinline__ BlockInfo get(const IndexerParams &p, int b) const {
+    const int i = b - b_lo;
+    if (i >= 0 && i < n) {
+      const int4 e0 = *reinterpret_cast<const int4 *>(tab + i * 8);
+      const int4 e1 = *reinterpret_cast<const int4 *>(tab + i * 8 + 4);
+      BlockInfo bi;
+      bi.first = e0.x;
+      bi.nrows = e0.y;
+      bi.req = e0.z;
+      bi.lmax = e0.w;
+      bi.lens[0] = e1.x;
+      bi.lens[1] = e1.y;
+      bi.lens[2] = e1.z;
+      bi.lens[3] = e1.w;
+      return bi;
+    }
+    return load_block(p, b);
   }
 };
 
@@ -140,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *sb = smem_raw + (base - raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = lay.stages, NQ = lay.nq, HP = lay.hp, NMAX = lay.n_max;
+  const int S = lay.stages, NQ = lay.nq, HP = lay.hp, NMAX = lay.n_max, NACC = lay.nacc;
   constexpr int kParts = F8 ? 2 : 1;              // fp8: hi and lo query terms
   const uint32_t qpartB = static_cast<uint32_t>(NMAX) * RB * ATOMS;
   const uint32_t qbufB = qpartB * kParts;
@@ -149,14 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *wbuf = reinterpret_cast<float *>(sb + lay.off_w);            // [NQ][NMAX]
   int *prefix = reinterpret_cast<int *>(sb + lay.off_prefix);         // [R + 1]
   const uint32_t bar0 = base + lay.off_bar;
-  // barrier map: full[S] empty[S] qfull[2] qempty[2] tfull[2] tempty[2] done
+  // barrier map: full[S] empty[S] qfull[2] qempty[2] tfull[4] tempty[4] done
   auto FULL = [&](int s) { return bar0 + 8u * s; };
   auto EMPTY = [&](int s) { return bar0 + 8u * (S + s); };
   auto QFULL = [&](int q) { return bar0 + 8u * (2 * S + q); };
   auto QEMPTY = [&](int q) { return bar0 + 8u * (2 * S + 2 + q); };
   auto TFULL = [&](int a) { return bar0 + 8u * (2 * S + 4 + a); };
-  auto TEMPTY = [&](int a) { return bar0 + 8u * (2 * S + 6 + a); };
-  const uint32_t DONE = bar0 + 8u * (2 * S + 8);
+  auto TEMPTY = [&](int a) { return bar0 + 8u * (2 * S + 8 + a); };
+  const uint32_t DONE = bar0 + 8u * (2 * S + 12);
   int *misc = reinterpret_cast<int *>(sb + lay.off_misc);  // [0] tmem base [1] abort [2..33] scan
   volatile int *abort_flag = misc + 1;
 
@@ -216,6 +262,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int beg = static_cast<int>((static_cast<long long>(blockIdx.x) * total) / gridDim.x);
   const int end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total) / gridDim.x);
   if (beg >= end) return;  // uniform across the CTA
+  BlockCache bc;
+  bc.tab = reinterpret_cast<int *>(sb + lay.off_blk);
+  bc.b_lo = find_block(prefix, R, beg);
+  {
+    const int nb = find_block(prefix, R, end - 1) - bc.b_lo + 1;
+    bc.n = nb < kBlkCache ? nb : kBlkCache;
+    for (int i = tid; i < bc.n; i += kThreads) {
+      const int b = bc.b_lo + i;
+      if (prefix[b + 1] > prefix[b]) {  // only blocks with tiles passed the checks above
+        const BlockInfo bi = load_block(p, b);
+        *reinterpret_cast<int4 *>(const_cast<int *>(bc.tab) + i * 8) = make_int4(bi.first, bi.nrows, bi.req, bi.lmax);
+        *reinterpret_cast<int4 *>(const_cast<int *>(bc.tab) + i * 8 + 4) =
+            make_int4(bi.lens[0], bi.lens[1], bi.lens[2], bi.lens[3]);
+      }
+    }
+  }
 
   // ---- barriers and tensor memory
   if (tid == 0) {
@@ -226,8 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < 2; ++q) {
       tc::mbar_init(QFULL(q), 1);
       tc::mbar_init(QEMPTY(q), 1 + 8);  // MMA commit + 8 epilogue warps
-      tc::mbar_init(TFULL(q), 1);
-      tc::mbar_init(TEMPTY(q), 4);      // the 4 warps of the owning warpgroup
+    }
+    for (int a = 0; a < 4; ++a) {
+      tc::mbar_init(TFULL(a), 1);
+      tc::mbar_init(TEMPTY(a), 4);      // the 4 warps of the owning warpgroup
     }
     tc::mbar_init(DONE, 1);
     tc::fence_mbar_init();
@@ -253,16 +317,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t policy = tc::l2_evict_first_policy();
     const uint64_t qpolicy = tc::l2_evict_last_policy();
     int cur = -1, qcount = -1, issued = 0;
+    int ps = 0, pphase = 0;  // ring position and phase of the next tile
+    int qstaged = 0;         // query stagings issued
     int win_base = 0, win_page = -1;  // page ids win_base + lane, held by lane
+    int nxt_base = -64, nxt_page = -1;  // the following window, loaded ahead
     BlockInfo bi{};
     const int32_t *pt = nullptr;
     for (; wk.valid(); wk.next()) {
       if (wk.block != cur) {
         cur = wk.block;
         ++qcount;
-        bi = load_block(p, cur);
+        bi = bc.get(p, cur);
         pt = p.page_table + static_cast<size_t>(bi.req) * p.max_pages_per_req;
         win_base = -64;  // force a window load for the new block
+        nxt_base = -64;
         const int qb = qcount % NQ;
         if (!warp_wait(QEMPTY(qb), ((qcount / NQ) & 1) ^ 1, abort_flag)) {
           if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
@@ -273,15 +341,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *wdst = wbuf + qb * NMAX;
         if constexpr (!F8) {
           // bf16: one TMA box per (row, K atom) writes the swizzled operand
-          // directly; the weights are loaded by the lanes meanwhile
-          for (int n = lane; n < NMAX; n += 32) {
-            const int rr = n / HP, h = n % HP;
-            const bool live = rr < bi.nrows && h < p.idx_heads;
-            wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] : 0.f;
+          // directly; when the head count needs no padding the block's weight
+          // rows are contiguous and one bulk copy brings them on the same
+          // barrier, else the lanes load them (the producer then waits for
+          // those loads)
+          const bool wbulk = p.idx_heads == HP;
+          if (!wbulk) {
+            for (int n = lane; n < NMAX; n += 32) {
+              const int rr = n / HP, h = n % HP;
+              const bool live = rr < bi.nrows && h < p.idx_heads;
+              wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] : 0.f;
+            }
+            __syncwarp();
           }
-          __syncwarp();
           if (lane == 0) {
-            tc::mbar_arrive_expect_tx(QFULL(qb), static_cast<uint32_t>(bi.nrows) * ATOMS * HP * RB);
+            const uint32_t wbytes = wbulk ? static_cast<uint32_t>(bi.nrows * HP) * 4u : 0u;
+            tc::mbar_arrive_expect_tx(QFULL(qb), static_cast<uint32_t>(bi.nrows) * ATOMS * HP * RB + wbytes);
+            if (wbulk)
+              tc::bulk_load(smem_u32(wdst), p.w + static_cast<size_t>(bi.first) * p.idx_heads, wbytes, QFULL(qb),
+                            qpolicy);
             for (int rr = 0; rr < bi.nrows; ++rr)
 #pragma unroll
               for (int a = 0; a < ATOMS; ++a)
@@ -337,11 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(QFULL(qb));
         }
+        ++qstaged;
       }
       {
-        const int it = wk.item - beg;
-        const int s = it % S;
-        if (!warp_wait(EMPTY(s), ((it / S) & 1) ^ 1, abort_flag)) {
+        const int s = ps;
+        if (!warp_wait(EMPTY(s), pphase ^ 1, abort_flag)) {
           if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
           break;
         }
@@ -358,8 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (k < npg) {
             const int pi = wk.tile() * npg + k;
             if (pi >= win_base + 32 || pi < win_base) {
-              win_base = pi;
-              win_page = win_base + lane < np_blk ? pt[win_base + lane] : -1;
+              if (pi == nxt_base) {
+                win_base = nxt_base;
+                win_page = nxt_page;
+              } else {
+                win_base = pi;
+                win_page = win_base + lane < np_blk ? pt[win_base + lane] : -1;
+              }
+              // load the next window now: it is used 32 pages from here
+              nxt_base = win_base + 32;
+              nxt_page = nxt_base + lane < np_blk ? pt[nxt_base + lane] : -1;
             }
             const int pg = __shfl_sync(0xFFFFFFFFu, win_page, pi - win_base);
             if (pi < np_blk) {
@@ -386,42 +472,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                             FULL(s), policy);
         }
         ++issued;
+        if (++ps == S) { ps = 0; pphase ^= 1; }
       }
       __syncwarp();
     }
-    // no copy may land after the CTA exits: wait for the last stages issued
-    if (lane == 0)
+    // no copy may land after the CTA exits: wait for the last stages and
+    // query buffers issued
+    if (lane == 0) {
       for (int it = max(0, issued - S); it < issued; ++it)
         tc::mbar_wait(FULL(it % S), (it / S) & 1, nullptr, kWaitBudget);
+      for (int qc = max(0, qstaged - NQ); qc < qstaged; ++qc)
+        tc::mbar_wait(QFULL(qc % NQ), (qc / NQ) & 1, nullptr, kWaitBudget);
+    }
     __syncwarp();
   } else if (warp == 1) {
     // ============================================================ MMA
     if (lane == 0) {
-      int cur = -1, qcount = -1, qb = 0, nrows = 1;
+      // One thread issues everything, so the loop is kept short: the
+      // descriptors' start-address field is linear in the shared-memory
+      // address (every operand lies below 256 KiB), so they are formed once
+      // and advanced by adding offsets >> 4; ring stage, accumulator and
+      // phases are running counters.
+      int cur = -1, qcount = -1, qb = 0;
+      int ms = 0, msphase = 0, ma = 0, maphase = 0;  // ring stage and accumulator of the next tile
+      const uint64_t adesc0 = make_desc<RB>(stage0);
+      const uint32_t batomD = static_cast<uint32_t>(NMAX * RB) >> 4, qpartD = qpartB >> 4;
+      uint64_t ad_s = adesc0, bd_q = 0;
+      uint32_t d = tmem, idesc = 0;
       bool any = false;
       for (; wk.valid(); wk.next()) {
-        const int it = wk.item - beg;
-        const int s = it % S, ab = it & 1;
+        const int s = ms, ab = ma;
         if (wk.block != cur) {
           cur = wk.block;
           ++qcount;
           qb = qcount % NQ;
-          nrows = p.block_nrows[cur];
+          idesc = tc::idesc_m128(HP * bc.get(p, cur).nrows, F8);
+          bd_q = make_desc<RB>(q0 + qb * qbufB);
           if (!tc::mbar_wait(QFULL(qb), (qcount / NQ) & 1, abort_flag, kWaitBudget)) break;
         }
-        if (!tc::mbar_wait(TEMPTY(ab), ((it >> 1) & 1) ^ 1, abort_flag, kWaitBudget)) break;
-        if (!tc::mbar_wait(FULL(s), (it / S) & 1, abort_flag, kWaitBudget)) break;
+        if (!tc::mbar_wait(TEMPTY(ab), maphase ^ 1, abort_flag, kWaitBudget)) break;
+        if (!tc::mbar_wait(FULL(s), msphase, abort_flag, kWaitBudget)) break;
         tc::tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(ab * NMAX);
-        const uint32_t idesc = tc::idesc_m128(HP * nrows, F8);
 #pragma unroll
         for (int a = 0; a < ATOMS; ++a)
 #pragma unroll
           for (int k = 0; k < kKsteps; ++k) {
-            const uint64_t ad = make_desc<RB>(stage0 + s * kStageB + a * kAtomB + k * 32);
+            const uint64_t ad = ad_s + static_cast<uint32_t>((a * kAtomB + k * 32) >> 4);
 #pragma unroll
             for (int part = 0; part < kParts; ++part) {
-              const uint64_t bd = make_desc<RB>(q0 + qb * qbufB + part * qpartB + a * NMAX * RB + k * 32);
+              const uint64_t bd = bd_q + (part * qpartD + a * batomD + static_cast<uint32_t>(k * 2));
               tc::mma<F8>(d, ad, bd, idesc, (a | k | part) != 0 ? 1u : 0u);
             }
           }
@@ -429,6 +528,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_commit(TFULL(ab));
         if (wk.last_of_block()) tc::mma_commit(QEMPTY(qb));
         any = true;
+        if (++ms == S) {
+          ms = 0;
+          msphase ^= 1;
+          ad_s = adesc0;
+        } else {
+          ad_s += kStageB >> 4;
+        }
+        if (++ma == NACC) {
+          ma = 0;
+          maphase ^= 1;
+          d = tmem;
+        } else {
+          d += static_cast<uint32_t>(NMAX);
+        }
       }
       if (wk.valid()) {
         *abort_flag = 1;
@@ -442,29 +555,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ======================================================= epilogue
-    const int wg = (warp - 2) >> 2;  // warpgroup: owns accumulator buffer wg
+    const int wg = (warp - 2) >> 2;  // warpgroup: owns the accumulator buffers of parity wg
     const int quarter = warp & 3;    // TMEM lanes 32*quarter .. +31
     const int tl = quarter * 32 + lane;
     int cur = -1, qcount = -1, qb = 0;
+    int ea = 0, eaphase = 0;  // accumulator buffer and phase of the next tile
     BlockInfo bi{};
     const int32_t *pt = nullptr;
     for (; wk.valid(); wk.next()) {
       const int it = wk.item - beg;
-      const int ab = it & 1;
+      const int ab = ea;
+      const int aphase = eaphase;
+      if (++ea == NACC) { ea = 0; eaphase ^= 1; }
       if (wk.block != cur) {
         if (cur >= 0 && lane == 0) tc::mbar_arrive(QEMPTY(qb));  // done with the old weights
         cur = wk.block;
         ++qcount;
         qb = qcount % NQ;
-        bi = load_block(p, cur);
+        bi = bc.get(p, cur);
         pt = p.page_table + static_cast<size_t>(bi.req) * p.max_pages_per_req;
         if (!warp_wait(QFULL(qb), (qcount / NQ) & 1, abort_flag)) {
           if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
           break;
         }
       }
-      if (ab != wg) continue;  // the other warpgroup's tile
-      if (!warp_wait(TFULL(ab), (it >> 1) & 1, abort_flag)) {
+      if ((it & 1) != wg) continue;  // the other warpgroup's tile
+      if (!warp_wait(TFULL(ab), aphase, abort_flag)) {
         if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
         break;
       }
@@ -563,8 +679,11 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
   lay.hp = (cfg.idx_heads + 15) & ~15;
   lay.n_max = lay.hp * cfg.block_rows;
   if (lay.n_max > 256 || cfg.max_rows > kMaxRowsTc) return cudaErrorInvalidValue;
+  // four accumulator buffers when they fit in TMEM: the MMA of tile i then
+  // waits for the epilogue of tile i - 4, not i - 2
+  lay.nacc = 4 * lay.n_max <= 512 ? 4 : 2;
   int cols = 32;
-  while (cols < 2 * lay.n_max) cols <<= 1;
+  while (cols < lay.nacc * lay.n_max) cols <<= 1;
   lay.tmem_cols = cols;
   // One CTA per SM: the deep key ring (up to 6 stages of 32 KiB) hides the
   // MMA/epilogue round trip; the floor keeps a second CTA (and a second TMEM
@@ -577,8 +696,9 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
   auto fixed = [&](int nq) {
     uint32_t off = nq * qbufB;                    // query buffers (after the stages)
     off += nq * lay.n_max * 4;                    // weights
-    off += (cfg.max_rows + 1) * 4 + 8;            // prefix table
-    off += (2 * 8 + 9) * 8 + 64;                  // barriers (upper bound) + misc
+    off += (cfg.max_rows + 1) * 4 + 16;           // prefix table
+    off += kBlkCache * 8 * 4;                     // block cache
+    off += (2 * 8 + 13) * 8 + 64;                 // barriers (upper bound) + misc
     return off + 1024 + 34 * 4;                   // alignment slack, scan scratch
   };
   lay.nq = 2;
@@ -597,9 +717,11 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
   off += lay.nq * lay.n_max * 4;
   lay.off_prefix = off;
   off += (cfg.max_rows + 1) * 4;
-  off = (off + 7u) & ~7u;
+  off = (off + 15u) & ~15u;
+  lay.off_blk = off;
+  off += kBlkCache * 8 * 4;
   lay.off_bar = off;
-  off += (2 * stages + 9) * 8;
+  off += (2 * stages + 13) * 8;
   lay.off_misc = off;
   off += 34 * 4;
   size_t smem = off + 1024;
