@@ -6,8 +6,9 @@
 // style; commit message 8: probabilities enter the value reduction in fp32.
 //
 // sparse_attn_kernel: persistent CTAs walk the (row, split) work items.  Warp
-// 0 is the gather producer: its lanes resolve 8 selected slots at a time
-// (slot -> position -> page -> row offset, bounds-checked) and issue one
+// 0 is the gather producer: its lanes resolve 32 selected slots at a time
+// (slot -> position -> page -> row offset, bounds-checked), two rounds ahead
+// of the copies so the dependent loads never stall the ring, and issue one
 // cp.async.bulk per token for its K row and one for its V row (all KV heads
 // of a token are contiguous, Hkv*D*2 bytes), into a ring of shared-memory
 // stages that complete on mbarriers.  Warps 1..Hkv are consumers, one per KV
@@ -142,6 +143,69 @@ __device__ __forceinline__ RowSplit row_split(const AttnParams &p, int item, boo
   return x;
 }
 
+// One round of the gather: up to 32 consecutive selected slots [base,
+// min(base + 32, b)) of one item (row split), lane j holding slot base + j.
+struct GatherRound {
+  bool valid;
+  int item, base, b, L;
+  const int32_t *sel, *pt;
+};
+
+__device__ __forceinline__ GatherRound round_at(const AttnParams &p, int item, int items, int lane) {
+  GatherRound d;
+  d.valid = false;
+  d.base = d.b = d.L = 0;
+  d.sel = d.pt = nullptr;
+  for (d.item = item; d.item < items; d.item += gridDim.x) {  // the next item with slots
+    const RowSplit x = row_split(p, d.item, lane == 0);
+    if (x.a < x.b) {
+      d.valid = true;
+      d.base = x.a;
+      d.b = x.b;
+      d.L = x.L;
+      d.sel = p.topk_idx + static_cast<size_t>(x.r) * p.topk;
+      d.pt = p.page_table + static_cast<size_t>(x.req) * p.max_pages_per_req;
+      break;
+    }
+  }
+  return d;
+}
+__device__ __forceinline__ GatherRound first_round(const AttnParams &p, int item, int items, int lane) {
+  return round_at(p, item, items, lane);
+}
+__device__ __forceinline__ GatherRound next_round(const AttnParams &p, GatherRound d, int items, int lane) {
+  if (!d.valid) return d;
+  if (d.base + 4 * kTokA < d.b) {
+    d.base += 4 * kTokA;
+    return d;
+  }
+  return round_at(p, d.item + gridDim.x, items, lane);
+}
+// The selected position of this lane's slot (-1: none).
+__device__ __forceinline__ int load_slot(const GatherRound &d, int lane) {
+  const int i = d.base + lane;
+  return d.valid && i < d.b ? d.sel[i] : -1;
+}
+// The page id holding position t, loaded only for a position inside the row.
+__device__ __forceinline__ int load_page(const AttnParams &p, const GatherRound &d, int t) {
+  return t >= 0 && t < d.L ? d.pt[t / p.page_size] : -1;
+}
+// Element offset of the token row of position t on page pg, or -1 (slot
+// unused or out of bounds; the bounds cases are flagged).
+__device__ __forceinline__ long long resolve_slot(const AttnParams &p, const GatherRound &d, int t, int pg,
+                                                  long long tok_stride) {
+  if (t == -1) return -1;
+  if (t < 0 || t >= d.L) {
+    flag_status(p.status, DSA_DEV_BAD_INDEX);
+    return -1;
+  }
+  if (pg < 0 || pg >= p.num_pages) {
+    flag_status(p.status, DSA_DEV_BAD_PAGE);
+    return -1;
+  }
+  return (static_cast<long long>(pg) * p.page_size + (t % p.page_size)) * tok_stride;
+}
+
 __device__ __forceinline__ bool warp_wait_a(uint32_t bar, uint32_t parity, const volatile int *abort_flag) {
   const bool ok = tc::mbar_wait(bar, parity, abort_flag, kWaitBudgetA);
   return __all_sync(0xFFFFFFFFu, ok);
@@ -179,53 +243,50 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
 
   if (warp == 0) {
     // ====================================================== gather producer
+    // Rounds of up to 32 selected slots (one item = one row split) are
+    // resolved ahead of their copies: while round A's stages are issued, the
+    // page ids of round B and the top-k slots of round C are in flight, so
+    // the two dependent loads per slot (slot -> position -> page) never stall
+    // the ring.
     const uint64_t policy = tc::l2_evict_first_policy();
     int chunk = 0;  // global chunk counter (ring position)
     bool stop = false;
-    for (int item = blockIdx.x; item < items && !stop; item += gridDim.x) {
-      const RowSplit x = row_split(p, item, lane == 0);
-      const int32_t *sel = p.topk_idx + static_cast<size_t>(x.r) * p.topk;
-      const int32_t *pt = p.page_table + static_cast<size_t>(x.req) * p.max_pages_per_req;
-      // resolve 32 slots per round (one L2 round trip for the indices and
-      // one for the page ids), then issue them as 4 stages of 8 tokens
-      for (int base = x.a; base < x.b && !stop; base += 4 * kTokA) {
-        long long off = -1;  // element offset of the token row
-        const int i = base + lane;
-        if (i < x.b) {
-          const int t = sel[i];
-          if (t != -1) {
-            if (t < 0 || t >= x.L) {
-              flag_status(p.status, DSA_DEV_BAD_INDEX);
-            } else {
-              const int page = pt[t / p.page_size];
-              if (page < 0 || page >= p.num_pages)
-                flag_status(p.status, DSA_DEV_BAD_PAGE);
-              else
-                off = (static_cast<long long>(page) * p.page_size + (t % p.page_size)) * tok_stride;
-            }
-          }
+    GatherRound dA = first_round(p, blockIdx.x, items, lane);
+    GatherRound dB = next_round(p, dA, items, lane);
+    GatherRound dC = next_round(p, dB, items, lane);
+    int tA = load_slot(dA, lane);
+    int tB = load_slot(dB, lane);
+    int tC = load_slot(dC, lane);
+    int pgA = load_page(p, dA, tA);
+    long long offA = resolve_slot(p, dA, tA, pgA, tok_stride);
+    while (dA.valid && !stop) {
+      const int pgB = load_page(p, dB, tB);  // lands while round A is issued
+      for (int sub = 0; sub < 4 && dA.base + sub * kTokA < dA.b; ++sub, ++chunk) {
+        const int st = chunk % NST;
+        if (!warp_wait_a(EMPTY(st), ((chunk / NST) & 1) ^ 1, abort_flag)) {
+          if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+          stop = true;
+          break;
         }
-        for (int sub = 0; sub < 4 && base + sub * kTokA < x.b; ++sub, ++chunk) {
-          const int st = chunk % NST;
-          if (!warp_wait_a(EMPTY(st), ((chunk / NST) & 1) ^ 1, abort_flag)) {
-            if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
-            stop = true;
-            break;
-          }
-          const bool mine = (lane >> 3) == sub;
-          if (mine) tok_ok[st * kTokA + (lane & 7)] = off >= 0 ? 1 : 0;
-          const uint32_t valid = __ballot_sync(0xFFFFFFFFu, mine && off >= 0);
-          __syncwarp();
-          if (lane == 0)
-            tc::mbar_arrive_expect_tx(FULL(st), static_cast<uint32_t>(__popc(valid)) * 2u * lay.row_bytes);
-          __syncwarp();
-          if (mine && off >= 0) {
-            const uint32_t dk = sbase + st * stageB + (lane & 7) * pitch;
-            tc::bulk_load(dk, p.k_cache + off * 2, lay.row_bytes, FULL(st), policy);
-            tc::bulk_load(dk + kTokA * pitch, p.v_cache + off * 2, lay.row_bytes, FULL(st), policy);
-          }
+        const bool mine = (lane >> 3) == sub;
+        if (mine) tok_ok[st * kTokA + (lane & 7)] = offA >= 0 ? 1 : 0;
+        const uint32_t valid = __ballot_sync(0xFFFFFFFFu, mine && offA >= 0);
+        __syncwarp();
+        if (lane == 0)
+          tc::mbar_arrive_expect_tx(FULL(st), static_cast<uint32_t>(__popc(valid)) * 2u * lay.row_bytes);
+        __syncwarp();
+        if (mine && offA >= 0) {
+          const uint32_t dk = sbase + st * stageB + (lane & 7) * pitch;
+          tc::bulk_load(dk, p.k_cache + offA * 2, lay.row_bytes, FULL(st), policy);
+          tc::bulk_load(dk + kTokA * pitch, p.v_cache + offA * 2, lay.row_bytes, FULL(st), policy);
         }
       }
+      offA = resolve_slot(p, dB, tB, pgB, tok_stride);
+      dA = dB;
+      dB = dC;
+      tB = tC;
+      dC = next_round(p, dC, items, lane);
+      tC = load_slot(dC, lane);
     }
     // drain: no copy may land after the CTA exits
     if (lane == 0)
