@@ -560,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tl = quarter * 32 + lane;
     int cur = -1, qcount = -1, qb = 0;
     int ea = 0, eaphase = 0;  // accumulator buffer and phase of the next tile
+    const uint64_t keep = tc::l2_evict_last_policy();
     BlockInfo bi{};
     const int32_t *pt = nullptr;
     for (; wk.valid(); wk.next()) {
@@ -627,7 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rr == i) L = bi.lens[i];
         if (t < L) {
           const float score = sum * sc;
-          p.scores[static_cast<size_t>(bi.first + rr) * p.score_width + t] = score;
+          // kept in L2 for the top-k that reads them next (the key stream is evict-first)
+          tc::st_global_hint(p.scores + static_cast<size_t>(bi.first + rr) * p.score_width + t, score, keep);
           if (p.row_hist != nullptr)  // first-level histogram for the top-k that follows
             atomicAdd(p.row_hist + static_cast<size_t>(bi.first + rr) * kKeyBins + (order_key(score) >> 20), 1u);
         }

@@ -147,7 +147,12 @@ __device__ __forceinline__ uint32_t radix_pass(TopkShared &sh, const uint32_t *k
   return min(sh.digit, static_cast<uint32_t>(kBins2 - 1));
 }
 
+// NG: 4-key groups per thread the launch provides for (a power of two >= the
+// segment's groups), so the unrolled per-group loops hold only the groups a
+// segment can have.
+template <int NG>
 __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkParams p) {
+  constexpr int NW = (NG + 3) / 4;  // 32-bit words of 8-bit per-group fields
   extern __shared__ __align__(16) uint8_t smem_raw[];
   TopkShared &sh = *reinterpret_cast<TopkShared *>(smem_raw);
   uint32_t *keys_s = reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(TopkShared) + 15) & ~size_t(15)));
@@ -179,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   const int seg = (((L + C - 1) / C) + 127) & ~127;
   const int lo = min(L, q * seg);
   const int n = min(L, lo + seg) - lo;
-  const int ng = (n + 4 * kThreads - 1) / (4 * kThreads);  // <= kGroupsMax
+  const int ng = (n + 4 * kThreads - 1) / (4 * kThreads);  // <= NG
   const float *srow = p.scores + static_cast<size_t>(r) * p.score_width + lo;
 
   // ---- A. the row's histogram and this segment's keys
@@ -190,14 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   }
   if ((p.score_width & 3) == 0) {
     const int n4 = n >> 2;
-    float4 v[kGroupsMax];
+    float4 v[NG];
 #pragma unroll
-    for (int u = 0; u < kGroupsMax; ++u) {
+    for (int u = 0; u < NG; ++u) {
       const int i4 = u * kThreads + tid;
       if (u < ng) v[u] = i4 < n4 ? __ldg(reinterpret_cast<const float4 *>(srow) + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kGroupsMax; ++u) {
+    for (int u = 0; u < NG; ++u) {
       const int i4 = u * kThreads + tid;
       if (u < ng) {
         uint4 k = make_uint4(0u, 0u, 0u, 0u);
@@ -227,7 +232,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
     part = warp_sum(part);
     if (lane == 0) sh.scan[warp] = part;
   }
-  if (tid == 0) sh.count = 0u;
   __syncthreads();  // keys, row histogram, scan
   if (!recount) {
     uint32_t total = 0u;
@@ -259,10 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   const bool checked = d1 == 0;  // the NaN bin is in play: the padding must not count
 
   if (in_bin <= static_cast<uint32_t>(kCandMax)) {
-    uint32_t hits[kGroupsMax];
+    uint32_t hits[NG];
     uint32_t nh = 0u;
 #pragma unroll
-    for (int u = 0; u < kGroupsMax; ++u) {
+    for (int u = 0; u < NG; ++u) {
       hits[u] = 0u;
       if (u < ng) {
         const uint4 kk = keys4[u * kThreads + tid];
@@ -275,12 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
         nh += __popc(hits[u]);
       }
     }
+    // offsets from a block scan of the per-thread counts (no shared atomics)
     const uint32_t incl = warp_incl_scan(nh, lane);
-    uint32_t base = 0u;
-    if (lane == 31 && incl) base = atomicAdd(&sh.count, incl);  // one atomic per warp
-    base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - nh;
+    if (lane == 31) sh.scan[warp] = incl;
+    __syncthreads();
+    const uint32_t wt = sh.scan[lane];  // warp lane's total
+    const uint32_t wincl = warp_incl_scan(wt, lane);
+    uint32_t base = __shfl_sync(0xFFFFFFFFu, wincl - wt, warp) + incl - nh;
+    if (tid == kThreads - 1) sh.count = base + nh;
 #pragma unroll
-    for (int u = 0; u < kGroupsMax; ++u) {
+    for (int u = 0; u < NG; ++u) {
       if (u < ng && hits[u]) {
         const uint4 kk = keys4[u * kThreads + tid];
         const uint32_t ks[4] = {kk.x, kk.y, kk.z, kk.w};
@@ -355,9 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   // per group: this thread's (keys > tau) << 16 | (keys == tau), and the
   // exclusive prefix of those counts over the warp's lanes (8-bit fields:
   // a warp holds at most 128 keys of a group)
-  uint32_t sel_gt[kGroupsMax / 4] = {}, sel_eq[kGroupsMax / 4] = {};
+  uint32_t sel_gt[NW] = {}, sel_eq[NW] = {};
 #pragma unroll
-  for (int u = 0; u < kGroupsMax; ++u) {
+  for (int u = 0; u < NG; ++u) {
     if (u < ng) {
       const uint4 kk = keys4[u * kThreads + tid];
       const uint32_t ks[4] = {kk.x, kk.y, kk.z, kk.w};
@@ -372,9 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
       sel_eq[u >> 2] |= e << (8 * (u & 3));
     }
   }
-  uint32_t ex_gt[kGroupsMax / 4], ex_eq[kGroupsMax / 4];
+  uint32_t ex_gt[NW], ex_eq[NW];
 #pragma unroll
-  for (int w4 = 0; w4 < kGroupsMax / 4; ++w4) {
+  for (int w4 = 0; w4 < NW; ++w4) {
     if (w4 * 4 < ng) {
       const uint32_t ig = warp_incl_scan(sel_gt[w4], lane), ie = warp_incl_scan(sel_eq[w4], lane);
       ex_gt[w4] = ig - sel_gt[w4];
@@ -414,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
     e_cta += *cl.map_shared_rank(&sh.cta_eq, rr);
   }
 #pragma unroll
-  for (int u = 0; u < kGroupsMax; ++u) {
+  for (int u = 0; u < NG; ++u) {
     if (u < ng) {
       const uint32_t before = sh.gbase[u] + sh.wtot[u][warp];
       uint32_t g = g_cta + (before >> 16) + ((ex_gt[u >> 2] >> (8 * (u & 3))) & 0xFFu);
@@ -450,12 +458,14 @@ cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, cudaStream
   const int C = topk_cluster_size(cfg.score_width);
   const int seg_w = (((cfg.score_width + C - 1) / C) + 127) & ~127;
   if (seg_w > kSegMax) return cudaErrorInvalidValue;
-  const int keys_w = (seg_w + 4 * kThreads - 1) / (4 * kThreads) * (4 * kThreads);  // whole groups
-  const size_t smem = ((sizeof(TopkShared) + 15) & ~size_t(15)) + static_cast<size_t>(keys_w) * 4;
-  cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  const int groups = (seg_w + 4 * kThreads - 1) / (4 * kThreads);
+  const int ng = groups <= 1 ? 1 : groups <= 2 ? 2 : groups <= 4 ? 4 : 8;
+  const size_t smem = ((sizeof(TopkShared) + 15) & ~size_t(15)) + static_cast<size_t>(ng) * 4 * kThreads * 4;
+  auto k = ng == 1 ? topk_cluster_kernel<1> : ng == 2 ? topk_cluster_kernel<2>
+           : ng == 4 ? topk_cluster_kernel<4> : topk_cluster_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  e = launch_pdl(topk_cluster_kernel, dim3(static_cast<unsigned>(cfg.max_rows * C)), dim3(kThreads), smem, st,
+  e = launch_pdl(k, dim3(static_cast<unsigned>(cfg.max_rows * C)), dim3(kThreads), smem, st,
                  static_cast<unsigned>(C), p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
