@@ -90,7 +90,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 dsa_status_t set_error(dsa_status_t st, const char *fmt, ...);
 
 // Each launcher returns the launch error (cudaSuccess when queued).
-cudaError_t launch_indexer(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st);
 cudaError_t launch_indexer_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st);
 cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, cudaStream_t st);
 cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cudaStream_t st);
