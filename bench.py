@@ -79,9 +79,12 @@ def describe(wl, cfg, step_bytes, flush=False) -> dict:
         "l2": f"inputs larger than L2: each step streams {step_bytes / 2**20:.0f} MiB of index keys and K/V "
               f"({step_bytes / 129e6:.1f}x the 129 MB L2)"
               + ("; plus a 256 MiB L2 flush between steps" if flush else ""),
-        "timing": "K CUDA-graph replays of dsa_step back to back between two CUDA events on the replay "
-                  "stream, divided by K; the per-kernel table comes from a second loop over the same four "
-                  "launches with event nodes between them",
+        "timing": ("one CUDA-graph replay of dsa_step per step between CUDA events, the L2 flush outside them"
+                   if flush else
+                   "K CUDA-graph replays of dsa_step back to back between two CUDA events on the replay "
+                   "stream, divided by K")
+                  + "; the per-kernel table comes from a second loop over the same four launches with event "
+                    "nodes between them",
     }
 
 
@@ -416,9 +419,9 @@ def run_dsa(args):
             step_graph.replay()
         step_ev[1].record(stream)
         stream.synchronize()
-        ms_back_to_back = step_ev[0].elapsed_time(step_ev[1]) / args.steps
+        ms_back_to_back = step_ev[0].elapsed_time(step_ev[1]) / args.steps  # flushes included when --flush
         wall_s = time.perf_counter() - t_wall
-        for k in range(min(args.steps, 200)):  # one replay at a time, launch latency included
+        for k in range(args.steps if args.flush else min(args.steps, 200)):  # one replay at a time
             if args.flush:
                 flush.fill_(k & 0xFF)
             step_ev[0].record(stream)
@@ -454,7 +457,9 @@ def run_dsa(args):
                 for i in range(4):
                     per_kernel[i].append(ev[i].elapsed_time(ev[i + 1]))
 
-    ms_step = ms_back_to_back
+    # with --flush the flush writes sit between the replays, so the step is
+    # timed one replay at a time (events around the replay only)
+    ms_step = statistics.mean(per_step) if args.flush else ms_back_to_back
     ms_local = torch.tensor([ms_step], dtype=torch.float64, device="cuda")
     if world > 1:
         dist.all_reduce(ms_local, op=dist.ReduceOp.MAX)

@@ -8,7 +8,8 @@
 //
 // Each fp32 score maps to a 32-bit key whose unsigned order is the ranking
 // (NaN -> 0, -0 -> +0).  A row is split across a cluster of C CTAs (1024
-// threads each, C = ceil(W / 16K) up to 8), each holding its contiguous
+// threads each, C = ceil(W / 16K) up to 8, or ceil(W / 32K) when the rows
+// outnumber what the GPU holds at once), each holding its contiguous
 // segment of the row as keys in shared memory.  Thread t of a CTA owns the
 // 4-key groups t, t + 1024, t + 2048, ... of the segment, so every pass over
 // the keys is a short fixed loop of 16-byte shared-memory reads, and a
@@ -30,6 +31,8 @@
 //     ascending position order.
 // Integer work only, so the result is bit-exact and deterministic.
 #include <cooperative_groups.h>
+
+#include <algorithm>
 
 #include "dsa_common.cuh"
 
@@ -449,13 +452,22 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
 
 }  // namespace
 
-int topk_cluster_size(int score_width) {
-  int c = (score_width + kSegPerCta - 1) / kSegPerCta;
-  return c < 1 ? 1 : (c > kMaxCluster ? kMaxCluster : c);
+// CTAs per row: ceil(W / 16K) (up to 8) keeps one row's chain short when the
+// rows' clusters fit on the GPU at once; with more rows than that, the
+// fewest CTAs the shared memory allows (ceil(W / 32K)) finish the batch in
+// fewer waves.
+int topk_cluster_size(int score_width, int max_rows) {
+  const int c_min = std::max(1, (score_width + kSegMax - 1) / kSegMax);
+  int c = std::max(c_min, std::min(kMaxCluster, (score_width + kSegPerCta - 1) / kSegPerCta));
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      static_cast<long long>(max_rows) * c > sms)
+    c = c_min;
+  return c;
 }
 
 cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, cudaStream_t st) {
-  const int C = topk_cluster_size(cfg.score_width);
+  const int C = topk_cluster_size(cfg.score_width, cfg.max_rows);
   const int seg_w = (((cfg.score_width + C - 1) / C) + 127) & ~127;
   if (seg_w > kSegMax) return cudaErrorInvalidValue;
   const int groups = (seg_w + 4 * kThreads - 1) / (4 * kThreads);
