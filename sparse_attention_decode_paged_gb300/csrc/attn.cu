@@ -23,7 +23,8 @@
 // Bytes in flight are set by the ring depth, not by registers.  Every wait is
 // bounded by an SM-clock budget; a wait that runs out sets DSA_DEV_TIMEOUT.
 //
-// merge_kernel: one warp per (row, head); combines the S partial states.
+// merge_kernel: one warp per (row, head), or per 2-8 of them when S is
+// small; combines the S partial states.
 #include <math.h>
 
 #include <algorithm>
@@ -104,13 +105,79 @@ __device__ __forceinline__ void merge_one(const float *part_m, const float *part
   if (lse && lane == 0) lse[rh] = lsum > 0.f ? mx + logf(lsum) : -INFINITY;
 }
 
-template <int D>
+// PPW (row, head) merges per warp when S <= kMergeRound / PPW: the warp's
+// PPW * S partial slices are contiguous (layout [R*Hq, S, D]) and all issued
+// in one round, so a small S does not leave the warp one short round trip.
+// Lane j * SMAX + s holds m and l of split s of the warp's pair j.
+template <int D, int PPW>
+__device__ __forceinline__ void merge_multi(const MergeParams &p, long long rh0, long long total, int lane) {
+  constexpr int VN = D / 32;
+  constexpr int SMAX = kMergeRound / PPW;
+  using VecT = typename std::conditional<VN == 4, float4, float2>::type;
+  const int S = p.num_splits;
+  const int mj = lane / SMAX, msl = lane - mj * SMAX;  // this lane's (pair, split) for m and l
+  float lsv = 0.f, mrv = -INFINITY;
+  if (mj < PPW && msl < S && rh0 + mj < total) {
+    lsv = __ldcg(p.part_l + (rh0 + mj) * S + msl);
+    mrv = __ldcg(p.part_m + (rh0 + mj) * S + msl);
+  }
+  float v[PPW][SMAX][VN];
+#pragma unroll
+  for (int j = 0; j < PPW; ++j)
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s)
+      if (s < S && rh0 + j < total) {
+        const VecT t = __ldcg(reinterpret_cast<const VecT *>(p.part_acc + ((rh0 + j) * S + s) * D + lane * VN));
+        v[j][s][0] = t.x;
+        v[j][s][1] = t.y;
+        if constexpr (VN == 4) { v[j][s][2] = t.z; v[j][s][3] = t.w; }
+      }
+  const float msv = lsv > 0.f ? mrv : -INFINITY;  // an empty split carries no weight
+#pragma unroll
+  for (int j = 0; j < PPW; ++j) {
+    const long long rh = rh0 + j;
+    if (rh >= total) break;  // warp-uniform
+    float mx = mj == j ? msv : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    const float f = (mj != j || msv == -INFINITY) ? 0.f : __expf(msv - mx);
+    float lsum = lsv * f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+    float o[VN];
+#pragma unroll
+    for (int d = 0; d < VN; ++d) o[d] = 0.f;
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s) {
+      const float fs = __shfl_sync(0xFFFFFFFFu, f, j * SMAX + s);
+      if (s < S) {
+#pragma unroll
+        for (int d = 0; d < VN; ++d) o[d] = fmaf(fs, v[j][s][d], o[d]);
+      }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + rh * D + lane * VN;
+#pragma unroll
+    for (int d = 0; d < VN; d += 2)
+      *reinterpret_cast<__nv_bfloat162 *>(dst + d) = __floats2bfloat162_rn(o[d] * inv, o[d + 1] * inv);
+    if (p.lse && lane == 0) p.lse[rh] = lsum > 0.f ? mx + logf(lsum) : -INFINITY;
+  }
+}
+
+// Merges per warp for S splits (a power of two, so the kernels stay few).
+inline int merge_pairs_per_warp(int S) { return S <= 3 ? 8 : S <= 6 ? 4 : S <= 12 ? 2 : 1; }
+
+template <int D, int PPW>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   pdl_wait();  // the partials come from the attention kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long rh = static_cast<long long>(blockIdx.x) * 8 + warp;  // (row, head)
-  if (rh >= static_cast<long long>(p.max_rows) * p.num_q_heads) return;
-  merge_one<D>(p.part_m, p.part_l, p.part_acc, rh, p.num_splits, p.out, p.lse, lane);
+  const long long total = static_cast<long long>(p.max_rows) * p.num_q_heads;
+  const long long rh0 = (static_cast<long long>(blockIdx.x) * 8 + warp) * PPW;  // first (row, head)
+  if (rh0 >= total) return;
+  if constexpr (PPW == 1)
+    merge_one<D>(p.part_m, p.part_l, p.part_acc, rh0, p.num_splits, p.out, p.lse, lane);
+  else
+    merge_multi<D, PPW>(p, rh0, total, lane);
 }
 
 struct AttnLayout {
@@ -465,11 +532,18 @@ cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cud
 
 cudaError_t launch_merge(const dsa_config_t &cfg, const MergeParams &p, cudaStream_t st) {
   const long long pairs = static_cast<long long>(cfg.max_rows) * cfg.num_q_heads;
-  const unsigned blocks = static_cast<unsigned>((pairs + 7) / 8);
-  cudaError_t e;
-  if (cfg.head_dim == 128) e = launch_pdl(merge_kernel<128>, dim3(blocks), dim3(256), 0, st, 1u, p);
-  else if (cfg.head_dim == 64) e = launch_pdl(merge_kernel<64>, dim3(blocks), dim3(256), 0, st, 1u, p);
-  else return cudaErrorInvalidValue;
+  const int ppw = merge_pairs_per_warp(cfg.num_splits);
+  const unsigned blocks = static_cast<unsigned>((pairs + 8LL * ppw - 1) / (8LL * ppw));
+  void (*k)(const MergeParams) = nullptr;
+  if (cfg.head_dim == 128)
+    k = ppw == 8 ? merge_kernel<128, 8> : ppw == 4 ? merge_kernel<128, 4> : ppw == 2 ? merge_kernel<128, 2>
+                                                                                      : merge_kernel<128, 1>;
+  else if (cfg.head_dim == 64)
+    k = ppw == 8 ? merge_kernel<64, 8> : ppw == 4 ? merge_kernel<64, 4> : ppw == 2 ? merge_kernel<64, 2>
+                                                                                    : merge_kernel<64, 1>;
+  else
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(k, dim3(blocks), dim3(256), 0, st, 1u, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
