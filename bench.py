@@ -484,6 +484,13 @@ def run_dsa(args):
 
     # ---- end to end through the public API, host buffers
     e2e = run_e2e(args, dsa, dev, inp, stream, flush) if args.e2e_steps > 0 else None
+    try:
+        probe = run_read_probe(dev, nbytes["indexer"], stream)
+    except Exception as exc:  # a measurement aid; report, do not fail the run
+        probe = {"error": repr(exc)[:200]}
+    if "us" in probe:
+        for n in ("indexer", "sparse_attn"):  # same byte count; the attention gathers 2 KiB rows instead
+            kernel_table[n]["frac_of_read_probe"] = (nbytes[n] / (k_ms[n] * 1e-3) / 1e9) / probe["gbs"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -499,7 +506,7 @@ def run_dsa(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": describe(wl, cfg, nbytes["step"], args.flush),
         "rows_per_s": dev.rows["num_rows"] * world / (ms_max * 1e-3),
         "hbm_gbs_step": step_gbs, "step_roofline_frac": step_gbs / peak,
-        "roofline": roofline, "kernels": kernel_table, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roofline, "kernels": kernel_table, "read_probe": probe, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks, "gpu_launches": 4 * args.steps, "device_status": status,
         "isolated_step_us": {"median": statistics.median(per_step) * 1e3, "min": min(per_step) * 1e3,
                              "note": "one replay per synchronize, graph launch latency included"},
@@ -510,6 +517,43 @@ def run_dsa(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_read_probe(dev, nbytes_idx, stream, reps=25):
+    """A plain read of the pages the step's indexer streams (page-table order,
+    16-byte loads, 16 x 256 threads per SM, no shared memory): the read-only
+    stream rate this GPU reaches on those bytes, timed like the kernels (CUDA
+    events around one launch, median)."""
+    import ctypes
+    import torch
+    from sparse_attention_decode_paged_gb300 import build as B
+    lib = ctypes.CDLL(B.PROBE_LIB)
+    lib.dsa_probe_read_pages.restype = ctypes.c_int
+    wl = dev.inp["workload"]
+    page_bytes = wl.page_size * wl.idx_dim * (1 if wl.idx_key_dtype else 2)
+    pt = dev.t["page_table"].flatten()
+    pt = pt[pt >= 0]
+    npages = int(min(pt.numel(), max(1, nbytes_idx // page_bytes)))
+    order = pt[:npages].to(torch.int32).contiguous()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sink = torch.empty(16 * sms * 256 // 32, dtype=torch.int32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    times = []
+    for _ in range(reps):
+        ev[0].record(stream)
+        rc = lib.dsa_probe_read_pages(ctypes.c_void_p(dev.t["idx_cache"].data_ptr()), ctypes.c_void_p(order.data_ptr()),
+                                      npages, page_bytes, ctypes.c_void_p(sink.data_ptr()), 16, 256,
+                                      ctypes.c_void_p(stream.cuda_stream))
+        ev[1].record(stream)
+        stream.synchronize()
+        if rc != 0:
+            return {"error": f"cuda error {rc}"}
+        times.append(ev[0].elapsed_time(ev[1]))
+    t_us = statistics.median(times[5:]) * 1e3
+    nbytes = npages * page_bytes
+    return {"bytes": nbytes, "us": t_us, "gbs": nbytes / (t_us * 1e-6) / 1e9,
+            "what": "plain read of the indexer's key pages in page-table order, 16-byte loads, "
+                    "16x256 threads per SM, median of CUDA-event-timed launches"}
 
 
 def run_e2e(args, dsa, dev, inp, stream, flush):

@@ -23,6 +23,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 LIB = os.path.join(PKG, "libdsa.so")
 STAMP = LIB + ".stamp"
+# read-only stream probe (not part of the DSA path; only the benchmark loads it)
+PROBE_SRC = os.path.join(PKG, "probe", "read_stream.cu")
+PROBE_LIB = os.path.join(PKG, "libdsa_probe.so")
 
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -48,7 +51,7 @@ def _digest() -> str:
     h = hashlib.sha256()
     h.update(platform.machine().encode())
     h.update(" ".join(NVCC_FLAGS).encode())
-    for d in (CSRC, INCLUDE):
+    for d in (CSRC, INCLUDE, os.path.dirname(PROBE_SRC)):
         for f in sorted(os.listdir(d)):
             with open(os.path.join(d, f), "rb") as fh:
                 h.update(f.encode())
@@ -57,7 +60,7 @@ def _digest() -> str:
 
 
 def up_to_date() -> bool:
-    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
+    if not (os.path.exists(LIB) and os.path.exists(STAMP) and os.path.exists(PROBE_LIB)):
         return False
     with open(STAMP) as f:
         return f.read().strip() == _digest()
@@ -80,9 +83,19 @@ def build(verbose: bool = False, force: bool = False) -> str:
             print(r.stdout + r.stderr, file=sys.stderr)
         return obj
 
+    def build_probe():
+        tmp = PROBE_LIB + ".tmp"
+        cmd = [nvcc, "-shared", PROBE_SRC, "-o", tmp] + NVCC_FLAGS
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on the read probe:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, PROBE_LIB)
+
     srcs = sources()
-    with cf.ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
+    with cf.ThreadPoolExecutor(max(1, min(len(srcs) + 1, os.cpu_count() or 1))) as ex:
+        probe = ex.submit(build_probe)
         objs = list(ex.map(compile_one, srcs))
+        probe.result()
     tmp = LIB + ".tmp"
     cmd = [nvcc, "-shared", "-o", tmp] + objs + GENCODE
     r = subprocess.run(cmd, capture_output=True, text=True)

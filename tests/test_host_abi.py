@@ -149,3 +149,17 @@ def test_null_and_misaligned_pointers_are_rejected_before_launch(dsa_lib):
     args = [vp(16)] * 3 + [None] + [vp(16)] * 7 + [None]
     assert lib.dsa_indexer_scores(ctypes.byref(f8), *args) == dsa_lib.DSA_ERR_INVALID_ARG
     assert b"idx_scale" in lib.dsa_last_error()
+
+
+def test_read_probe_library_exports(dsa_lib):
+    """The benchmark's read-only stream probe is built beside the library
+    (its own .so, not part of the DSA path) and exports its one entry."""
+    import ctypes
+    from sparse_attention_decode_paged_gb300 import build as B
+
+    assert os.path.exists(B.PROBE_LIB)
+    lib = ctypes.CDLL(B.PROBE_LIB)
+    assert hasattr(lib, "dsa_probe_read_pages")
+    # host-side argument checks run before any device call
+    lib.dsa_probe_read_pages.restype = ctypes.c_int
+    assert lib.dsa_probe_read_pages(None, None, 1, 16, None, 1, 256, None) != 0
