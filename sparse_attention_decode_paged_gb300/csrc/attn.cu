@@ -446,11 +446,12 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
           a1 &= vmask;
           a2 &= vmask;
           a3 &= vmask;
-          mma_bf16_1688(o[mt], a0, a1, ph);
-          mma_bf16_1688(o[mt], a0, a1, pm);
+          // hi and mid in one k16 MMA: its K runs over (token, term) pairs,
+          // so the V^T fragment appears twice and P_hi, P_mid are the two
+          // halves of the B fragment; lo in a k8 MMA
+          mma_bf16_16816(o[mt], a0, a1, a0, a1, ph, pm);
           mma_bf16_1688(o[mt], a0, a1, pl);
-          mma_bf16_1688(o[mt + 1], a2, a3, ph);
-          mma_bf16_1688(o[mt + 1], a2, a3, pm);
+          mma_bf16_16816(o[mt + 1], a2, a3, a2, a3, ph, pm);
           mma_bf16_1688(o[mt + 1], a2, a3, pl);
         }
         __syncwarp();
