@@ -184,7 +184,7 @@ struct AttnLayout {
   int stages;
   int row_bytes;  // Hkv * D * 2: one token's K (or V) row, all KV heads
   int row_pitch;  // row_bytes + 16 in shared memory
-  uint32_t off_ok, off_p, off_a, off_bar, off_misc;
+  uint32_t off_ok, off_items, off_bar, off_misc;
 };
 
 struct RowSplit {
@@ -210,21 +210,45 @@ __device__ __forceinline__ RowSplit row_split(const AttnParams &p, int item, boo
   return x;
 }
 
+// The CTA's items (item k = blockIdx.x + k * gridDim.x), resolved once into
+// shared memory before the kernel waits for the top-k, so neither the
+// producer's look-ahead nor a consumer starting an item waits on the row
+// metadata loads: [kItemCache][8] = a, b, L, req, r, s.  Items past the
+// cache are resolved on the spot.
+constexpr int kItemCache = 64;
+
+__device__ __forceinline__ RowSplit item_split(const AttnParams &p, const int *tab, int ncache, int k, bool flag) {
+  if (k < ncache) {
+    const int4 e0 = *reinterpret_cast<const int4 *>(tab + 8 * k);
+    const int2 e1 = *reinterpret_cast<const int2 *>(tab + 8 * k + 4);
+    RowSplit x;
+    x.a = e0.x;
+    x.b = e0.y;
+    x.L = e0.z;
+    x.req = e0.w;
+    x.r = e1.x;
+    x.s = e1.y;
+    return x;
+  }
+  return row_split(p, blockIdx.x + k * gridDim.x, flag);
+}
+
 // One round of the gather: up to 32 consecutive selected slots [base,
 // min(base + 32, b)) of one item (row split), lane j holding slot base + j.
 struct GatherRound {
   bool valid;
-  int item, base, b, L;
+  int k, base, b, L;  // k: the item's index among this CTA's items
   const int32_t *sel, *pt;
 };
 
-__device__ __forceinline__ GatherRound round_at(const AttnParams &p, int item, int items, int lane) {
+__device__ __forceinline__ GatherRound round_at(const AttnParams &p, const int *tab, int ncache, int k, int nmine,
+                                                int lane) {
   GatherRound d;
   d.valid = false;
   d.base = d.b = d.L = 0;
   d.sel = d.pt = nullptr;
-  for (d.item = item; d.item < items; d.item += gridDim.x) {  // the next item with slots
-    const RowSplit x = row_split(p, d.item, lane == 0);
+  for (d.k = k; d.k < nmine; ++d.k) {  // the next item with slots
+    const RowSplit x = item_split(p, tab, ncache, d.k, lane == 0);
     if (x.a < x.b) {
       d.valid = true;
       d.base = x.a;
@@ -237,16 +261,14 @@ __device__ __forceinline__ GatherRound round_at(const AttnParams &p, int item, i
   }
   return d;
 }
-__device__ __forceinline__ GatherRound first_round(const AttnParams &p, int item, int items, int lane) {
-  return round_at(p, item, items, lane);
-}
-__device__ __forceinline__ GatherRound next_round(const AttnParams &p, GatherRound d, int items, int lane) {
+__device__ __forceinline__ GatherRound next_round(const AttnParams &p, const int *tab, int ncache, GatherRound d,
+                                                  int nmine, int lane) {
   if (!d.valid) return d;
   if (d.base + 4 * kTokA < d.b) {
     d.base += 4 * kTokA;
     return d;
   }
-  return round_at(p, d.item + gridDim.x, items, lane);
+  return round_at(p, tab, ncache, d.k + 1, nmine, lane);
 }
 // The selected position of this lane's slot (-1: none).
 __device__ __forceinline__ int load_slot(const GatherRound &d, int lane) {
@@ -302,10 +324,20 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     tc::fence_mbar_init();
   }
   pdl_launch_dependents();
+  // this CTA's items from the row metadata (not produced by the top-k, so
+  // read while the top-k still runs)
+  const int items = p.max_rows_attn * S;
+  const int nmine = static_cast<int>(blockIdx.x) < items ? (items - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+  const int ncache = min(nmine, kItemCache);
+  int *item_tab = reinterpret_cast<int *>(smem + lay.off_items);
+  for (int k = threadIdx.x; k < ncache; k += blockDim.x) {
+    const RowSplit x = row_split(p, blockIdx.x + k * gridDim.x, true);
+    *reinterpret_cast<int4 *>(item_tab + 8 * k) = make_int4(x.a, x.b, x.L, x.req);
+    *reinterpret_cast<int2 *>(item_tab + 8 * k + 4) = make_int2(x.r, x.s);
+  }
   pdl_wait();  // the selection comes from the top-k kernel
   __syncthreads();
 
-  const int items = p.max_rows_attn * S;
   const long long tok_stride = static_cast<long long>(Hkv) * D;  // elements per token row
 
   if (warp == 0) {
@@ -318,9 +350,9 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     const uint64_t policy = tc::l2_evict_first_policy();
     int chunk = 0;  // global chunk counter (ring position)
     bool stop = false;
-    GatherRound dA = first_round(p, blockIdx.x, items, lane);
-    GatherRound dB = next_round(p, dA, items, lane);
-    GatherRound dC = next_round(p, dB, items, lane);
+    GatherRound dA = round_at(p, item_tab, ncache, 0, nmine, lane);
+    GatherRound dB = next_round(p, item_tab, ncache, dA, nmine, lane);
+    GatherRound dC = next_round(p, item_tab, ncache, dB, nmine, lane);
     int tA = load_slot(dA, lane);
     int tB = load_slot(dB, lane);
     int tC = load_slot(dC, lane);
@@ -352,7 +384,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
       dA = dB;
       dB = dC;
       tB = tC;
-      dC = next_round(p, dC, items, lane);
+      dC = next_round(p, item_tab, ncache, dC, nmine, lane);
       tC = load_slot(dC, lane);
     }
     // drain: no copy may land after the CTA exits
@@ -365,8 +397,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     const int g = warp - 1;
     const int c4 = lane & 3, g4 = lane >> 2;  // g4: query head of the group (A row)
     int chunk = 0;
-    for (int item = blockIdx.x; item < items; item += gridDim.x) {
-      const RowSplit x = row_split(p, item, false);
+    for (int k = 0; k < nmine; ++k) {
+      const RowSplit x = item_split(p, item_tab, ncache, k, false);
       // A operand: this group's query heads (rows 8..15 are zero padding)
       uint32_t qa[D / 16][2];
 #pragma unroll
@@ -497,11 +529,9 @@ cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cud
   uint32_t off = static_cast<uint32_t>(stages) * stage_bytes;
   lay.off_ok = off;
   off += stages * kTokA * 4;
-  lay.off_p = off;
-  off += cfg.num_kv_heads * kTokA * 8 * 4;
-  lay.off_a = off;
-  off += cfg.num_kv_heads * 8 * 4;
   off = (off + 15u) & ~15u;
+  lay.off_items = off;
+  off += kItemCache * 8 * 4;
   lay.off_bar = off;
   off += 2 * stages * 8;
   lay.off_misc = off;
