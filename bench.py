@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["dsa", "reference"], default="dsa")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
     ap.add_argument("--splits", type=int, default=None, help="override the top-k split count")
+    ap.add_argument("--kv-layout", choices=["interleaved", "separate"], default="interleaved",
+                    help="K/V cache layout: one [pages, P, 2, Hkv, D] cache (default) or two [pages, P, Hkv, D]")
     ap.add_argument("--batch", type=int, default=None,
                     help="fewer decode requests (profiling captures only; the bench line uses the full batch)")
     ap.add_argument("--e2e-steps", type=int, default=30)
@@ -76,6 +78,8 @@ def describe(wl, cfg, step_bytes, flush=False) -> dict:
                     f"head dim {wl.head_dim} bf16",
         "batch": int(wl.max_reqs), "score_width": int(wl.score_width), "topk": int(wl.topk),
         "page_size": int(wl.page_size), "num_splits": int(cfg.num_splits),
+        "kv_layout": ("interleaved: one cache [pages, P, 2, Hkv, D], a token's K row then its V row"
+                      if cfg.flags & 2 else "separate K and V caches [pages, P, Hkv, D]"),
         "l2": f"inputs larger than L2: each step streams {step_bytes / 2**20:.0f} MiB of index keys and K/V "
               f"({step_bytes / 129e6:.1f}x the 129 MB L2)"
               + ("; plus a 256 MiB L2 flush between steps" if flush else ""),
@@ -338,6 +342,8 @@ def run_dsa(args):
     # the per-kernel calls below mirror dsa_step, which hands the indexer's
     # key histogram to the top-k
     override["flags"] = dsa.DSA_FLAG_TOPK_HISTOGRAM
+    if args.kv_layout == "interleaved":  # a token's K and V rows adjacent: one copy per selected token
+        override["flags"] |= dsa.DSA_FLAG_KV_INTERLEAVED
     dev = DeviceStep(inp, **override)
     cfg, t, v = dev.cfg, dev.t, dev.views
     gen_s = time.time() - t_gen

@@ -122,7 +122,15 @@ enum {
    * histogram with the right total that does not match the scores (the scores
    * changed in between) sets DSA_DEV_BAD_HIST and that row's selection is
    * unspecified.  No case reads or writes outside the buffers. */
-  DSA_FLAG_TOPK_HISTOGRAM = 1 << 0
+  DSA_FLAG_TOPK_HISTOGRAM = 1 << 0,
+  /* K and V of a token are adjacent in one cache: k_cache is
+   * [num_pages, page_size, 2, num_kv_heads, head_dim] bf16 (the token's K row
+   * for all KV heads, then its V row) and v_cache must equal
+   * k_cache + num_kv_heads * head_dim * 2 bytes (else DSA_ERR_INVALID_ARG).
+   * The sparse attention then moves each selected token with one copy
+   * instead of two; results are identical to the separate layout.  A layout
+   * of this library's own (the pages keep K and V apart). */
+  DSA_FLAG_KV_INTERLEAVED = 1 << 1
 };
 
 /* Every pointer one fused step needs (all device pointers). */

@@ -183,7 +183,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
 struct AttnLayout {
   int stages;
   int row_bytes;  // Hkv * D * 2: one token's K (or V) row, all KV heads
-  int row_pitch;  // row_bytes + 16 in shared memory
+  int tok_pitch;  // shared-memory stride between a stage's tokens (16 B of padding per row)
+  int v_off;      // offset of a token's V row from its K row in a stage
+  int stage_bytes;
   uint32_t off_ok, off_items, off_bar, off_misc;
 };
 
@@ -306,9 +308,9 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv, S = p.num_splits;
-  const int NST = lay.stages, pitch = lay.row_pitch;
+  const int NST = lay.stages, pitch = lay.tok_pitch;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t stageB = 2u * kTokA * pitch;                      // K block then V block
+  const uint32_t stageB = static_cast<uint32_t>(lay.stage_bytes);  // K block then V block, or [K|V] per token
   int *tok_ok = reinterpret_cast<int *>(smem + lay.off_ok);        // [NST][kTokA]
   const uint32_t bar0 = sbase + lay.off_bar;
   auto FULL = [&](int st) { return bar0 + 8u * st; };
@@ -338,7 +340,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
   pdl_wait();  // the selection comes from the top-k kernel
   __syncthreads();
 
-  const long long tok_stride = static_cast<long long>(Hkv) * D;  // elements per token row
+  const long long tok_stride = static_cast<long long>(Hkv) * D * (p.kv_interleaved ? 2 : 1);  // elements per token
 
   if (warp == 0) {
     // ====================================================== gather producer
@@ -376,8 +378,12 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
         __syncwarp();
         if (mine && offA >= 0) {
           const uint32_t dk = sbase + st * stageB + (lane & 7) * pitch;
-          tc::bulk_load(dk, p.k_cache + offA * 2, lay.row_bytes, FULL(st), policy);
-          tc::bulk_load(dk + kTokA * pitch, p.v_cache + offA * 2, lay.row_bytes, FULL(st), policy);
+          if (p.kv_interleaved) {  // the token's K and V rows in one copy
+            tc::bulk_load(dk, p.k_cache + offA * 2, 2u * lay.row_bytes, FULL(st), policy);
+          } else {
+            tc::bulk_load(dk, p.k_cache + offA * 2, lay.row_bytes, FULL(st), policy);
+            tc::bulk_load(dk + lay.v_off, p.v_cache + offA * 2, lay.row_bytes, FULL(st), policy);
+          }
         }
       }
       offA = resolve_slot(p, dB, tB, pgB, tok_stride);
@@ -469,7 +475,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
         uint32_t ph, pm, pl;
         split3_bf16x2(p0, p1, ph, pm, pl);
         const uint32_t vmask = (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
-        const uint32_t vaddr = kst + kTokA * pitch + tok * pitch + (g * D + (mat & 1) * 8 + (mat >> 1) * 16) * 2;
+        const uint32_t vaddr = kst + lay.v_off + tok * pitch + (g * D + (mat & 1) * 8 + (mat >> 1) * 16) * 2;
 #pragma unroll
         for (int mt = 0; mt < D / 16; mt += 2) {
           uint32_t a0, a1, a2, a3;
@@ -521,8 +527,16 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
 cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cudaStream_t st) {
   AttnLayout lay;
   lay.row_bytes = cfg.num_kv_heads * cfg.head_dim * 2;
-  lay.row_pitch = lay.row_bytes + 16;
-  const int stage_bytes = 2 * kTokA * lay.row_pitch;
+  if (p.kv_interleaved) {  // [K|V] per token
+    lay.tok_pitch = 2 * lay.row_bytes + 16;
+    lay.v_off = lay.row_bytes;
+    lay.stage_bytes = kTokA * lay.tok_pitch;
+  } else {  // the stage's K rows, then its V rows
+    lay.tok_pitch = lay.row_bytes + 16;
+    lay.v_off = kTokA * lay.tok_pitch;
+    lay.stage_bytes = 2 * kTokA * lay.tok_pitch;
+  }
+  const int stage_bytes = lay.stage_bytes;
   int stages = (100 * 1024) / stage_bytes;  // about 100 KB of ring: two CTAs per SM
   stages = stages < 2 ? 2 : (stages > kMaxStagesA ? kMaxStagesA : stages);
   lay.stages = stages;

@@ -134,7 +134,7 @@ dsa_status_t dsa_validate_config(const dsa_config_t *c) {
     return fail(DSA_ERR_INVALID_ARG, "idx_key_dtype %d unknown", c->idx_key_dtype);
   if (!(c->sm_scale > 0.f) || !std::isfinite(c->sm_scale))
     return fail(DSA_ERR_INVALID_ARG, "sm_scale must be positive and finite");
-  if ((c->flags & ~static_cast<int32_t>(DSA_FLAG_TOPK_HISTOGRAM)) != 0)
+  if ((c->flags & ~static_cast<int32_t>(DSA_FLAG_TOPK_HISTOGRAM | DSA_FLAG_KV_INTERLEAVED)) != 0)
     return fail(DSA_ERR_INVALID_ARG, "unknown flags 0x%x", c->flags);
   if (static_cast<long long>(c->max_reqs) * c->max_pages_per_req > 0x7FFFFFFFLL)
     return fail(DSA_ERR_INVALID_ARG, "page table larger than 2^31 entries");
@@ -333,6 +333,11 @@ dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void 
   DSA_CHECK_DEV_PTR(topk_idx);
   DSA_CHECK_DEV_PTR(part_m);
   DSA_CHECK_DEV_PTR(part_l);
+  const bool kv_interleaved = (cfg->flags & DSA_FLAG_KV_INTERLEAVED) != 0;
+  if (kv_interleaved &&
+      static_cast<const char *>(v_cache) !=
+          static_cast<const char *>(k_cache) + static_cast<size_t>(cfg->num_kv_heads) * cfg->head_dim * 2)
+    return fail(DSA_ERR_INVALID_ARG, "DSA_FLAG_KV_INTERLEAVED: v_cache must be k_cache + num_kv_heads*head_dim*2 bytes");
   DSA_CHECK_DEV_PTR(part_acc);
   DSA_CHECK_DEV_PTR(workspace);
   dsa::AttnParams p;
@@ -358,6 +363,7 @@ dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void 
   p.num_pages = cfg->num_pages;
   p.page_size = cfg->page_size;
   p.sm_scale_log2 = cfg->sm_scale * 1.4426950408889634f;
+  p.kv_interleaved = kv_interleaved ? 1 : 0;
   return cuda_status(dsa::launch_sparse_attn(*cfg, p, stream), "sparse attention launch");
 }
 

@@ -36,8 +36,8 @@ struct TopkParams {
 
 struct AttnParams {
   const uint8_t *q;        // bf16 [R, Hq, D]
-  const uint8_t *k_cache;  // bf16 [NP, P, Hkv, D]
-  const uint8_t *v_cache;
+  const uint8_t *k_cache;  // bf16 [NP, P, Hkv, D], or [NP, P, 2, Hkv, D] with V interleaved
+  const uint8_t *v_cache;  // k_cache + Hkv * D * 2 when interleaved
   const int32_t *page_table;
   const int32_t *row_req;
   const int32_t *row_len;
@@ -49,6 +49,7 @@ struct AttnParams {
   int32_t num_q_heads, num_kv_heads, topk, num_splits;
   int32_t max_rows_attn, max_reqs, max_pages_per_req, score_width, num_pages, page_size;
   float sm_scale_log2;     // sm_scale * log2(e)
+  int32_t kv_interleaved;  // 1: one copy moves a token's K and V rows
 };
 
 struct MergeParams {

@@ -36,6 +36,7 @@ DSA_KEY_BF16 = 0
 DSA_KEY_FP8_E4M3 = 1
 
 DSA_FLAG_TOPK_HISTOGRAM = 1 << 0
+DSA_FLAG_KV_INTERLEAVED = 1 << 1
 
 EXPORTED = (
     "dsa_validate_config", "dsa_workspace_size", "dsa_workspace_layout",
@@ -283,13 +284,26 @@ def dsa_topk(cfg, scores, row_len, topk_idx, workspace, stream=None) -> None:
         _dev(topk_idx, "topk_idx", (torch.int32,), R * cfg.topk), _ws(workspace), _stream(stream)))
 
 
+def _kv_ptrs(cfg, k_cache, v_cache):
+    """K and V cache pointers.  With DSA_FLAG_KV_INTERLEAVED, k_cache is the
+    one [num_pages, P, 2, Hkv, D] cache and the V pointer is derived from it
+    (v_cache may be None, or a view whose first element is the first V row)."""
+    kv = cfg.num_pages * cfg.page_size * cfg.num_kv_heads * cfg.head_dim
+    if cfg.flags & DSA_FLAG_KV_INTERLEAVED:
+        k = _dev(k_cache, "k_cache", _BF16, 2 * kv)
+        v = ctypes.c_void_p(k.value + cfg.num_kv_heads * cfg.head_dim * 2)
+        if v_cache is not None and v_cache.data_ptr() != v.value:
+            raise ValueError("v_cache: with DSA_FLAG_KV_INTERLEAVED it must start at k_cache's first V row")
+        return k, v
+    return _dev(k_cache, "k_cache", _BF16, kv), _dev(v_cache, "v_cache", _BF16, kv)
+
+
 def dsa_sparse_attn(cfg, q, k_cache, v_cache, page_table, row_req, row_len, topk_idx, part_m,
                     part_l, part_acc, workspace, stream=None) -> None:
     R, Hq, S, D = cfg.max_rows, cfg.num_q_heads, cfg.num_splits, cfg.head_dim
-    kv = cfg.num_pages * cfg.page_size * cfg.num_kv_heads * D
+    k_ptr, v_ptr = _kv_ptrs(cfg, k_cache, v_cache)
     _check(_lib.dsa_sparse_attn(
-        ctypes.byref(cfg), _dev(q, "q", _BF16, R * Hq * D), _dev(k_cache, "k_cache", _BF16, kv),
-        _dev(v_cache, "v_cache", _BF16, kv),
+        ctypes.byref(cfg), _dev(q, "q", _BF16, R * Hq * D), k_ptr, v_ptr,
         _dev(page_table, "page_table", (torch.int32,), cfg.max_reqs * cfg.max_pages_per_req),
         _dev(row_req, "row_req", (torch.int32,), R), _dev(row_len, "row_len", (torch.int32,), R),
         _dev(topk_idx, "topk_idx", (torch.int32,), R * cfg.topk),
@@ -329,9 +343,14 @@ def make_step_args(cfg, t: dict) -> dsa_step_args_t:
                 lse=(f32, R * Hq))
     a = dsa_step_args_t()
     for name in STEP_FIELDS:
+        if name in ("k_cache", "v_cache"):
+            continue
         dt, n = spec[name]
         p = _dev(t.get(name), name, dt, n)
         setattr(a, name, p.value if p is not None else None)
+    k_ptr, v_ptr = _kv_ptrs(cfg, t.get("k_cache"), t.get("v_cache"))
+    a.k_cache = k_ptr.value if k_ptr is not None else None
+    a.v_cache = v_ptr.value if v_ptr is not None else None
     return a
 
 

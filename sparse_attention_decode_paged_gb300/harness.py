@@ -47,6 +47,10 @@ class DeviceStep:
         t["q"] = to_device(inp["q"], device, "bf16")
         t["k_cache"] = to_device(inp["k_cache"], device, "bf16")
         t["v_cache"] = to_device(inp["v_cache"], device, "bf16")
+        if self.cfg.flags & dsa.DSA_FLAG_KV_INTERLEAVED:
+            # one cache [NP, P, 2, Hkv, D]: each token's K row, then its V row
+            kv = torch.stack((t["k_cache"], t["v_cache"]), dim=2).contiguous()
+            t["k_cache"], t["v_cache"] = kv, kv[:, :, 1]
         t["out"] = torch.zeros(R, Hq, D, dtype=torch.bfloat16, device=device)
         t["lse"] = torch.zeros(R, Hq, dtype=torch.float32, device=device)
         self.t = t

@@ -359,3 +359,29 @@ def test_topk_histogram_mismatch(dsa_lib, cuda_ok):
     torch.cuda.synchronize()
     assert dev.status() == 0
     assert torch.equal(v["topk_idx"], plain.views["topk_idx"])
+
+
+@pytest.mark.parametrize("i", [0, 1, 3])
+def test_kv_interleaved_layout_identical(i, dsa_lib, cuda_ok):
+    """DSA_FLAG_KV_INTERLEAVED (a token's K and V rows adjacent, one copy per
+    token) gives bit-identical outputs to the separate K and V caches."""
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    inp = W.generate(i)
+    sep = DeviceStep(inp)
+    itl = DeviceStep(inp, flags=dsa_lib.DSA_FLAG_KV_INTERLEAVED)
+    assert itl.t["k_cache"].shape[2] == 2
+    for dev in (sep, itl):
+        dev.step()
+    torch.cuda.synchronize()
+    assert sep.status() == 0 and itl.status() == 0
+    assert torch.equal(sep.t["out"], itl.t["out"])
+    assert torch.equal(sep.t["lse"], itl.t["lse"])
+    # the separate calls take the same layout
+    cfg, t, v = itl.cfg, itl.t, itl.views
+    v["part_acc"].zero_()
+    dsa_lib.dsa_sparse_attn(cfg, t["q"], t["k_cache"], None, t["page_table"], t["row_req"], t["row_len"],
+                            v["topk_idx"], v["part_m"], v["part_l"], v["part_acc"], itl.workspace)
+    dsa_lib.dsa_merge(cfg, v["part_m"], v["part_l"], v["part_acc"], t["out"], t["lse"])
+    torch.cuda.synchronize()
+    assert torch.equal(sep.t["out"], itl.t["out"])

@@ -163,3 +163,26 @@ def test_read_probe_library_exports(dsa_lib):
     # host-side argument checks run before any device call
     lib.dsa_probe_read_pages.restype = ctypes.c_int
     assert lib.dsa_probe_read_pages(None, None, 1, 16, None, 1, 256, None) != 0
+
+
+def test_kv_interleaved_requires_adjacent_v(dsa_lib):
+    """With DSA_FLAG_KV_INTERLEAVED the V pointer must be the K pointer plus
+    one K row; anything else is rejected before any launch."""
+    cfg = dsa_lib.make_config(num_q_heads=64, num_kv_heads=8, head_dim=128, idx_heads=64, idx_dim=128,
+                              page_size=64, topk=2048, num_splits=8, max_rows=64, max_reqs=64,
+                              max_pages_per_req=512, score_width=32768, num_pages=32768, block_rows=1,
+                              idx_key_dtype=0, flags=dsa_lib.DSA_FLAG_KV_INTERLEAVED)
+    lib = ctypes.CDLL(dsa_lib.LIB_PATH)
+    lib.dsa_sparse_attn.restype = ctypes.c_int
+    base = 0x10000000
+    p = [ctypes.c_void_p(base + 0x100000 * k) for k in range(12)]
+    row = 8 * 128 * 2
+    bad = lib.dsa_sparse_attn(ctypes.byref(cfg), p[0], p[1], ctypes.c_void_p(p[1].value + row + 16), p[3], p[4],
+                              p[5], p[6], p[7], p[8], p[9], p[10], None)
+    assert bad == dsa_lib.DSA_ERR_INVALID_ARG
+    assert "KV_INTERLEAVED" in lib_last_error(lib)
+
+
+def lib_last_error(lib):
+    lib.dsa_last_error.restype = ctypes.c_char_p
+    return lib.dsa_last_error().decode()
