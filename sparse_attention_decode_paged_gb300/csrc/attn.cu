@@ -10,8 +10,10 @@
 // (slot -> position -> page -> row offset, bounds-checked), two rounds ahead
 // of the copies so the dependent loads never stall the ring, and issue one
 // cp.async.bulk per token for its K row and one for its V row (all KV heads
-// of a token are contiguous, Hkv*D*2 bytes), into a ring of shared-memory
-// stages that complete on mbarriers.  Warps 1..Hkv are consumers, one per KV
+// of a token are contiguous, Hkv*D*2 bytes) — or, with the interleaved cache
+// layout, one copy for both (the producer's copy-issue rate, not the bytes,
+// bounds an L2-resident gather) — into a ring of shared-memory stages that
+// complete on mbarriers.  Warps 1..Hkv are consumers, one per KV
 // head g: scores on the tensor cores (mma.sync m16n8k16 with the group's <= 8
 // query heads as the A rows and 8 keys as N; key fragments by ldmatrix from
 // rows padded by 16 bytes so the 8 rows hit distinct banks), an online
