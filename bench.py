@@ -46,6 +46,27 @@ CPU_SAMPLE_ROWS = 2
 KERNEL_SOURCE = {"indexer": "indexer_tc.cu", "sparse_attn": "attn.cu"}  # file holding each timed kernel
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's value (the job's wall time is its slowest
+    rank's); a plain value when there is one rank.  Uses the process group's
+    backend device (CUDA tensors for NCCL, CPU tensors for gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job(ms_max: float, rows_per_rank: int, world: int) -> dict:
+    """Whole-job figures of N replicas that each run one full step at once:
+    µs per layer-step as the job delivers them (the slowest rank's time over
+    N) and rows per second over all ranks."""
+    return {"us_per_step": ms_max * 1e3 / world, "rows_per_s": rows_per_rank * world / (ms_max * 1e-3)}
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -466,10 +487,7 @@ def run_dsa(args):
     # with --flush the flush writes sit between the replays, so the step is
     # timed one replay at a time (events around the replay only)
     ms_step = statistics.mean(per_step) if args.flush else ms_back_to_back
-    ms_local = torch.tensor([ms_step], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(ms_local, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_local.item())
+    ms_max = max_over_ranks(ms_step, world)
 
     names = ["indexer", "topk", "sparse_attn", "merge"]
     k_ms = {n: statistics.mean(x) for n, x in zip(names, per_kernel)}
@@ -505,12 +523,13 @@ def run_dsa(args):
         except Exception as exc:  # report, do not fail the GPU measurement
             cpu = {"error": repr(exc)[:300]}
 
-    us = ms_max * 1e3 / world  # whole-job µs per layer-step (replicas run concurrently)
+    job = whole_job(ms_max, dev.rows["num_rows"], world)  # replicas run concurrently
+    us = job["us_per_step"]
     line = {
         "metric": METRIC, "value": us, "unit": "us", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": describe(wl, cfg, nbytes["step"], args.flush),
-        "rows_per_s": dev.rows["num_rows"] * world / (ms_max * 1e-3),
+        "rows_per_s": job["rows_per_s"],
         "hbm_gbs_step": step_gbs, "step_roofline_frac": step_gbs / peak,
         "roofline": roofline, "kernels": kernel_table, "read_probe": probe, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks, "gpu_launches": 4 * args.steps, "device_status": status,
