@@ -177,19 +177,6 @@ __device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
-// layout: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte
-// offset), start address in 16-byte units; version 1, swizzle mode 2.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);          // start address
-  d |= static_cast<uint64_t>(1u) << 16;                          // leading byte offset (unused)
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;                  // stride byte offset
-  d |= static_cast<uint64_t>(1u) << 46;                          // descriptor version
-  d |= static_cast<uint64_t>(2u) << 61;                          // 128-byte swizzle
-  return d;
-}
-
 // Instruction descriptor: fp32 accumulate, K-major A and B, M = 128.
 // kind::f16 with bf16 inputs (format 1) or kind::f8f6f4 with e4m3 (format 0).
 __host__ __device__ constexpr uint32_t idesc_m128(int n, bool f8) {
