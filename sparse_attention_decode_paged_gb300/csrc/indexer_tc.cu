@@ -104,6 +104,69 @@ __device__ __forceinline__ BlockInfo load_block(const IndexerParams &p, int b) {
   return bi;
 }
 
+// Stages a score block's fp8 queries: each query head x (bf16) becomes two
+// e4m3 terms hi + lo with one scale s = amax/448 (x/s = hi + lo, lo the e4m3
+// rounding of the residual), written swizzled as the MMA's two B parts, and
+// s folds into the head weight.  Threads t of nthr (a multiple of 32) work in
+// teams of kMembers per head, each on a share of the head's RB dims (whole
+// 16-byte e4m3 chunks); every thread of the participating warps must call it
+// (the teams reduce amax by shuffles).
+template <int RB>
+__device__ __forceinline__ void stage_q_fp8(const IndexerParams &p, const BlockInfo &bi, uint8_t *qdst,
+                                            uint32_t qpartB, float *wdst, int NMAX, int HP, int t, int nthr) {
+  constexpr int kMembers = RB / 16 < 4 ? RB / 16 : 4;
+  constexpr int kPart = RB / kMembers;  // dims (= e4m3 bytes) per team member, a multiple of 16
+  const int DIr = p.idx_dim;
+  const int team = t / kMembers, part = t % kMembers, nteams = nthr / kMembers;
+  for (int base = 0; base < NMAX; base += nteams) {  // same trip count in every lane
+    const int n = base + team;
+    const int rr = n / HP, h = n % HP;
+    const bool live = n < NMAX && rr < bi.nrows && h < p.idx_heads;
+    const uint8_t *src = p.q_idx + (static_cast<size_t>(bi.first + rr) * p.idx_heads + h) * DIr * 2;
+    uint4 v[kPart / 8];  // this member's kPart bf16 inputs
+#pragma unroll
+    for (int c = 0; c < kPart / 8; ++c) {
+      const int d0 = part * kPart + c * 8;
+      v[c] = (live && d0 < DIr) ? *reinterpret_cast<const uint4 *>(src + d0 * 2) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int c = 0; c < kPart / 8; ++c) {
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v[c].x)), fabsf(bf16hi(v[c].x))),
+                               fmaxf(fabsf(bf16lo(v[c].y)), fabsf(bf16hi(v[c].y)))));
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v[c].z)), fabsf(bf16hi(v[c].z))),
+                               fmaxf(fabsf(bf16lo(v[c].w)), fabsf(bf16hi(v[c].w)))));
+    }
+#pragma unroll
+    for (int o = 1; o < kMembers; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (n >= NMAX) continue;
+    const float sigma = amax > 0.f ? amax / 448.f : 1.f;
+    const float inv = 1.f / sigma;
+#pragma unroll
+    for (int c = 0; c < kPart / 16; ++c) {  // 16 e4m3 per 16-byte chunk
+      uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+      const uint32_t w8[8] = {v[2 * c].x, v[2 * c].y, v[2 * c].z, v[2 * c].w,
+                              v[2 * c + 1].x, v[2 * c + 1].y, v[2 * c + 1].z, v[2 * c + 1].w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float x0 = bf16lo(w8[k]) * inv, x1 = bf16hi(w8[k]) * inv;
+        const __nv_fp8x2_storage_t ph = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+        __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(ph, __NV_E4M3);
+        const float2 hf = __half22float2(*reinterpret_cast<__half2 *>(&hr));
+        const __nv_fp8x2_storage_t pl =
+            __nv_cvt_float2_to_fp8x2(make_float2(x0 - hf.x, x1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+        hi[k >> 1] |= static_cast<uint32_t>(ph) << (16 * (k & 1));
+        lo[k >> 1] |= static_cast<uint32_t>(pl) << (16 * (k & 1));
+      }
+      const uint32_t o = swizzle<RB>(n * RB + part * kPart + c * 16);
+      *reinterpret_cast<uint4 *>(qdst + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4 *>(qdst + qpartB + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    if (part == 0)
+      wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] * sigma : 0.f;
+  }
+}
+
 // The score block holding tile `item`: b with pf[b] <= item < pf[b+1].
 __device__ __forceinline__ int find_block(const int *pf, int nblocks, int item) {
   int lo = 0, hi = nblocks;
@@ -309,6 +372,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
+  // fp8 queries of the CTA's first NQ score blocks: quantised by all warps
+  // now, so the producer does not do it alone while its key ring drains
+  int npre = 0;
+  if constexpr (F8) {
+    int b = bc.b_lo;
+    for (int j = 0; j < NQ && b < R && prefix[b] < end; ++j) {
+      const BlockInfo bj = bc.get(p, b);
+      stage_q_fp8<RB>(p, bj, sb + lay.off_q + j * qbufB, qpartB, wbuf + j * NMAX, NMAX, HP, tid, kThreads);
+      ++npre;
+      do {  // the next block with tiles
+        ++b;
+      } while (b < R && prefix[b + 1] == prefix[b]);
+    }
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0)
+      for (int j = 0; j < npre; ++j) tc::mbar_arrive(QFULL(j));
+  }
+
   Walker wk;
   wk.start(prefix, R, beg, end);
 
@@ -332,88 +414,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         win_base = -64;  // force a window load for the new block
         nxt_base = -64;
         const int qb = qcount % NQ;
-        if (!warp_wait(QEMPTY(qb), ((qcount / NQ) & 1) ^ 1, abort_flag)) {
-          if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
-          break;
-        }
-        // stage the block's queries (B operand) and head weights
-        uint8_t *qdst = sb + lay.off_q + qb * qbufB;
-        float *wdst = wbuf + qb * NMAX;
-        if constexpr (!F8) {
-          // bf16: one TMA box per (row, K atom) writes the swizzled operand
-          // directly; when the head count needs no padding the block's weight
-          // rows are contiguous and one bulk copy brings them on the same
-          // barrier, else the lanes load them (the producer then waits for
-          // those loads)
-          const bool wbulk = p.idx_heads == HP;
-          if (!wbulk) {
-            for (int n = lane; n < NMAX; n += 32) {
-              const int rr = n / HP, h = n % HP;
-              const bool live = rr < bi.nrows && h < p.idx_heads;
-              wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] : 0.f;
-            }
-            __syncwarp();
+        if (qcount >= npre) {  // (the first npre were staged by the whole CTA before the loop)
+          if (!warp_wait(QEMPTY(qb), ((qcount / NQ) & 1) ^ 1, abort_flag)) {
+            if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+            break;
           }
-          if (lane == 0) {
-            const uint32_t wbytes = wbulk ? static_cast<uint32_t>(bi.nrows * HP) * 4u : 0u;
-            tc::mbar_arrive_expect_tx(QFULL(qb), static_cast<uint32_t>(bi.nrows) * ATOMS * HP * RB + wbytes);
-            if (wbulk)
-              tc::bulk_load(smem_u32(wdst), p.w + static_cast<size_t>(bi.first) * p.idx_heads, wbytes, QFULL(qb),
-                            qpolicy);
-            for (int rr = 0; rr < bi.nrows; ++rr)
-#pragma unroll
-              for (int a = 0; a < ATOMS; ++a)
-                tc::tma_load_2d(q0 + qb * qbufB + a * NMAX * RB + rr * HP * RB, &qmap, a * (RB / kElem),
-                                (bi.first + rr) * p.idx_heads, QFULL(qb), qpolicy);
-          }
-        } else {
-          // fp8: each query head becomes hi + lo e4m3 terms with one scale;
-          // the row's loads are issued together (unrolled) before any math
-          const int DIr = p.idx_dim;
-          for (int n = lane; n < NMAX; n += 32) {
-            const int rr = n / HP, h = n % HP;
-            const bool live = rr < bi.nrows && h < p.idx_heads;
-            const uint8_t *src = p.q_idx + (static_cast<size_t>(bi.first + rr) * p.idx_heads + h) * DIr * 2;
-            float amax = 0.f;
-            uint4 v[RB / 8];  // the whole row: RB e4m3 values = RB bf16 inputs
-#pragma unroll
-            for (int c = 0; c < RB / 8; ++c)
-              v[c] = (live && c * 8 < DIr) ? *reinterpret_cast<const uint4 *>(src + c * 16) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int c = 0; c < RB / 8; ++c) {
-              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v[c].x)), fabsf(bf16hi(v[c].x))),
-                                       fmaxf(fabsf(bf16lo(v[c].y)), fabsf(bf16hi(v[c].y)))));
-              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v[c].z)), fabsf(bf16hi(v[c].z))),
-                                       fmaxf(fabsf(bf16lo(v[c].w)), fabsf(bf16hi(v[c].w)))));
-            }
-            const float sigma = amax > 0.f ? amax / 448.f : 1.f;
-            const float inv = 1.f / sigma;
-#pragma unroll
-            for (int c = 0; c < RB / 16; ++c) {  // 16 e4m3 per 16-byte chunk
-              uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
-              const uint32_t w8[8] = {v[2 * c].x, v[2 * c].y, v[2 * c].z, v[2 * c].w,
-                                      v[2 * c + 1].x, v[2 * c + 1].y, v[2 * c + 1].z, v[2 * c + 1].w};
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const float x0 = bf16lo(w8[k]) * inv, x1 = bf16hi(w8[k]) * inv;
-                const __nv_fp8x2_storage_t ph =
-                    __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
-                __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(ph, __NV_E4M3);
-                const float2 hf = __half22float2(*reinterpret_cast<__half2 *>(&hr));
-                const __nv_fp8x2_storage_t pl =
-                    __nv_cvt_float2_to_fp8x2(make_float2(x0 - hf.x, x1 - hf.y), __NV_SATFINITE, __NV_E4M3);
-                hi[k >> 1] |= static_cast<uint32_t>(ph) << (16 * (k & 1));
-                lo[k >> 1] |= static_cast<uint32_t>(pl) << (16 * (k & 1));
+          // stage the block's queries (B operand) and head weights
+          uint8_t *qdst = sb + lay.off_q + qb * qbufB;
+          float *wdst = wbuf + qb * NMAX;
+          if constexpr (!F8) {
+            // bf16: one TMA box per (row, K atom) writes the swizzled operand
+            // directly; when the head count needs no padding the block's weight
+            // rows are contiguous and one bulk copy brings them on the same
+            // barrier, else the lanes load them (the producer then waits for
+            // those loads)
+            const bool wbulk = p.idx_heads == HP;
+            if (!wbulk) {
+              for (int n = lane; n < NMAX; n += 32) {
+                const int rr = n / HP, h = n % HP;
+                const bool live = rr < bi.nrows && h < p.idx_heads;
+                wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] : 0.f;
               }
-              const uint32_t o = swizzle<RB>(n * RB + c * 16);
-              *reinterpret_cast<uint4 *>(qdst + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-              *reinterpret_cast<uint4 *>(qdst + qpartB + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+              __syncwarp();
             }
-            wdst[n] = live ? p.w[static_cast<size_t>(bi.first + rr) * p.idx_heads + h] * sigma : 0.f;
+            if (lane == 0) {
+              const uint32_t wbytes = wbulk ? static_cast<uint32_t>(bi.nrows * HP) * 4u : 0u;
+              tc::mbar_arrive_expect_tx(QFULL(qb), static_cast<uint32_t>(bi.nrows) * ATOMS * HP * RB + wbytes);
+              if (wbulk)
+                tc::bulk_load(smem_u32(wdst), p.w + static_cast<size_t>(bi.first) * p.idx_heads, wbytes, QFULL(qb),
+                              qpolicy);
+              for (int rr = 0; rr < bi.nrows; ++rr)
+#pragma unroll
+                for (int a = 0; a < ATOMS; ++a)
+                  tc::tma_load_2d(q0 + qb * qbufB + a * NMAX * RB + rr * HP * RB, &qmap, a * (RB / kElem),
+                                  (bi.first + rr) * p.idx_heads, QFULL(qb), qpolicy);
+            }
+          } else {
+            // fp8: each query head becomes hi + lo e4m3 terms with one scale
+            stage_q_fp8<RB>(p, bi, qdst, qpartB, wdst, NMAX, HP, lane, 32);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(QFULL(qb));
           }
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(QFULL(qb));
         }
         ++qstaged;
       }
