@@ -372,23 +372,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
-  // fp8 queries of the CTA's first NQ score blocks: quantised by all warps
-  // now, so the producer does not do it alone while its key ring drains
+  // fp8 queries of the CTA's first NQ score blocks: quantised now by warps
+  // 1..9 (warp 0, the producer, starts streaming keys meanwhile), so the
+  // producer does not do it alone while its key ring drains
   int npre = 0;
   if constexpr (F8) {
     int b = bc.b_lo;
     for (int j = 0; j < NQ && b < R && prefix[b] < end; ++j) {
-      const BlockInfo bj = bc.get(p, b);
-      stage_q_fp8<RB>(p, bj, sb + lay.off_q + j * qbufB, qpartB, wbuf + j * NMAX, NMAX, HP, tid, kThreads);
+      if (warp != 0)
+        stage_q_fp8<RB>(p, bc.get(p, b), sb + lay.off_q + j * qbufB, qpartB, wbuf + j * NMAX, NMAX, HP, tid - 32,
+                        kThreads - 32);
       ++npre;
       do {  // the next block with tiles
         ++b;
       } while (b < R && prefix[b + 1] == prefix[b]);
     }
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0)
-      for (int j = 0; j < npre; ++j) tc::mbar_arrive(QFULL(j));
+    if (warp != 0) {
+      tc::fence_proxy_async_smem();
+      asm volatile("bar.sync 1, %0;\n" ::"r"(kThreads - 32) : "memory");  // warps 1..9 only
+      if (tid == 32)
+        for (int j = 0; j < npre; ++j) tc::mbar_arrive(QFULL(j));
+    }
   }
 
   Walker wk;
