@@ -409,12 +409,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nxt_base = -64, nxt_page = -1;  // the following window, loaded ahead
     BlockInfo bi{};
     const int32_t *pt = nullptr;
+    const int P = p.page_size;
+    const int npg = kTok / P;  // pages per tile: 1, 2, 4 or 8
+    int np_blk = 0;            // pages of the current block up to its longest row
     for (; wk.valid(); wk.next()) {
       if (wk.block != cur) {
         cur = wk.block;
         ++qcount;
         bi = bc.get(p, cur);
         pt = p.page_table + static_cast<size_t>(bi.req) * p.max_pages_per_req;
+        np_blk = (bi.lmax + P - 1) / P;
         win_base = -64;  // force a window load for the new block
         nxt_base = -64;
         const int qb = qcount % NQ;
@@ -470,50 +474,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         // page ids of this tile from a 32-entry window the whole warp loads
-        // at once (one L2 round trip per 32 pages instead of one per page)
-        const int P = p.page_size;
-        const int npg = kTok / P;
-        const int np_blk = (bi.lmax + P - 1) / P;
-        int pages[8];
-        int nvalid = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          pages[k] = -1;
-          if (k < npg) {
-            const int pi = wk.tile() * npg + k;
-            if (pi >= win_base + 32 || pi < win_base) {
-              if (pi == nxt_base) {
-                win_base = nxt_base;
-                win_page = nxt_page;
-              } else {
-                win_base = pi;
-                win_page = win_base + lane < np_blk ? pt[win_base + lane] : -1;
-              }
-              // load the next window now: it is used 32 pages from here
-              nxt_base = win_base + 32;
-              nxt_page = nxt_base + lane < np_blk ? pt[nxt_base + lane] : -1;
-            }
-            const int pg = __shfl_sync(0xFFFFFFFFu, win_page, pi - win_base);
-            if (pi < np_blk) {
-              if (pg >= 0 && pg < p.num_pages) {
-                pages[k] = pg;
-                ++nvalid;
-              } else if (lane == 0) {
-                flag_status(p.status, DSA_DEV_BAD_PAGE);
-              }
-            }
+        // at once (one L2 round trip per 32 pages instead of one per page);
+        // lane k < npg resolves the tile's page k.  Windows start at
+        // multiples of npg and 32 % npg == 0, so a tile never straddles two.
+        const int pi0 = wk.tile() * npg;
+        if (pi0 >= win_base + 32 || pi0 < win_base) {
+          if (pi0 == nxt_base) {
+            win_base = nxt_base;
+            win_page = nxt_page;
+          } else {
+            win_base = pi0;
+            win_page = win_base + lane < np_blk ? pt[win_base + lane] : -1;
           }
+          // load the next window now: it is used 32 pages from here
+          nxt_base = win_base + 32;
+          nxt_page = nxt_base + lane < np_blk ? pt[nxt_base + lane] : -1;
         }
-        if (lane == 0) tc::mbar_arrive_expect_tx(FULL(s), static_cast<uint32_t>(nvalid) * P * RB * ATOMS);
+        const int pi = pi0 + (lane < npg ? lane : 0);
+        const int pgl = __shfl_sync(0xFFFFFFFFu, win_page, pi - win_base);
+        const bool inblk = lane < npg && pi < np_blk;
+        const bool okp = inblk && pgl >= 0 && pgl < p.num_pages;
+        const uint32_t okm = __ballot_sync(0xFFFFFFFFu, okp);
+        if (__ballot_sync(0xFFFFFFFFu, inblk && !okp) != 0u && lane == 0) flag_status(p.status, DSA_DEV_BAD_PAGE);
+        if (lane == 0)
+          tc::mbar_arrive_expect_tx(FULL(s), static_cast<uint32_t>(__popc(okm)) * P * RB * ATOMS);
         __syncwarp();
         // one lane per (page, K atom) box: the boxes of a tile are issued in parallel
         {
           const int k = lane / ATOMS, a = lane % ATOMS;
-          int pg = -1;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            if (kk == k) pg = pages[kk];
-          if (lane < npg * ATOMS && pg >= 0)
+          const int pg = __shfl_sync(0xFFFFFFFFu, pgl, k & 31);
+          if (lane < npg * ATOMS && ((okm >> k) & 1u))
             tc::tma_load_2d(stage0 + s * kStageB + a * kAtomB + k * P * RB, &kmap, a * (RB / kElem), pg * P,
                             FULL(s), policy);
         }
