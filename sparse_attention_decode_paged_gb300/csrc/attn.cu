@@ -281,7 +281,7 @@ __device__ __forceinline__ int load_slot(const GatherRound &d, int lane) {
 }
 // The page id holding position t, loaded only for a position inside the row.
 __device__ __forceinline__ int load_page(const AttnParams &p, const GatherRound &d, int t) {
-  return t >= 0 && t < d.L ? d.pt[t / p.page_size] : -1;
+  return t >= 0 && t < d.L ? d.pt[t >> p.page_shift] : -1;
 }
 // Element offset of the token row of position t on page pg, or -1 (slot
 // unused or out of bounds; the bounds cases are flagged).
@@ -296,7 +296,7 @@ __device__ __forceinline__ long long resolve_slot(const AttnParams &p, const Gat
     flag_status(p.status, DSA_DEV_BAD_PAGE);
     return -1;
   }
-  return (static_cast<long long>(pg) * p.page_size + (t % p.page_size)) * tok_stride;
+  return (static_cast<long long>(pg) * p.page_size + (t & (p.page_size - 1))) * tok_stride;
 }
 
 __device__ __forceinline__ bool warp_wait_a(uint32_t bar, uint32_t parity, const volatile int *abort_flag) {
@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     // the ring.
     const uint64_t policy = tc::l2_evict_first_policy();
     int chunk = 0;  // global chunk counter (ring position)
+    int pst = 0, pph = 0;  // its ring stage and phase
     bool stop = false;
     GatherRound dA = round_at(p, item_tab, ncache, 0, nmine, lane);
     GatherRound dB = next_round(p, item_tab, ncache, dA, nmine, lane);
@@ -365,8 +366,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     while (dA.valid && !stop) {
       const int pgB = load_page(p, dB, tB);  // lands while round A is issued
       for (int sub = 0; sub < 4 && dA.base + sub * kTokA < dA.b; ++sub, ++chunk) {
-        const int st = chunk % NST;
-        if (!warp_wait_a(EMPTY(st), ((chunk / NST) & 1) ^ 1, abort_flag)) {
+        const int st = pst;
+        if (!warp_wait_a(EMPTY(st), pph ^ 1, abort_flag)) {
           if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
           stop = true;
           break;
@@ -387,6 +388,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
             tc::bulk_load(dk + lay.v_off, p.v_cache + offA * 2, lay.row_bytes, FULL(st), policy);
           }
         }
+        if (++pst == NST) { pst = 0; pph ^= 1; }
       }
       offA = resolve_slot(p, dB, tB, pgB, tok_stride);
       dA = dB;
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     // ============================================ consumers: one per KV head
     const int g = warp - 1;
     const int c4 = lane & 3, g4 = lane >> 2;  // g4: query head of the group (A row)
-    int chunk = 0;
+    int cst = 0, cph = 0;  // ring stage and phase of the next chunk
     for (int k = 0; k < nmine; ++k) {
       const RowSplit x = item_split(p, item_tab, ncache, k, false);
       // A operand: this group's query heads (rows 8..15 are zero padding)
@@ -424,9 +426,9 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       bool aborted = false;
-      for (int base = x.a; base < x.b; base += kTokA, ++chunk) {
-        const int st = chunk % NST;
-        if (!warp_wait_a(FULL(st), (chunk / NST) & 1, abort_flag)) {
+      for (int base = x.a; base < x.b; base += kTokA) {
+        const int st = cst;
+        if (!warp_wait_a(FULL(st), cph, abort_flag)) {
           if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
           aborted = true;
           break;
@@ -496,6 +498,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(EMPTY(st));
+        if (++cst == NST) { cst = 0; cph ^= 1; }
       }
       if (aborted) break;
       // partial state of heads g*G .. g*G+G-1 for this split

@@ -364,6 +364,8 @@ dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void 
   p.page_size = cfg->page_size;
   p.sm_scale_log2 = cfg->sm_scale * 1.4426950408889634f;
   p.kv_interleaved = kv_interleaved ? 1 : 0;
+  p.page_shift = 0;
+  while ((1 << p.page_shift) < cfg->page_size) ++p.page_shift;  // page_size is a validated power of two
   return cuda_status(dsa::launch_sparse_attn(*cfg, p, stream), "sparse attention launch");
 }
 

@@ -50,6 +50,7 @@ struct AttnParams {
   int32_t max_rows_attn, max_reqs, max_pages_per_req, score_width, num_pages, page_size;
   float sm_scale_log2;     // sm_scale * log2(e)
   int32_t kv_interleaved;  // 1: one copy moves a token's K and V rows
+  int32_t page_shift;      // log2(page_size)
 };
 
 struct MergeParams {
