@@ -145,8 +145,11 @@ typedef struct {
   const void *idx_cache;      /* bf16 or e4m3 [num_pages, page_size, idx_dim]      */
   const float *idx_scale;     /* fp32 [num_pages, page_size], NULL for bf16 keys   */
   const void *q;              /* bf16 [max_rows, num_q_heads, head_dim]            */
-  const void *k_cache;        /* bf16 [num_pages, page_size, num_kv_heads, head_dim] */
-  const void *v_cache;        /* bf16, same shape as k_cache                      */
+  const void *k_cache;        /* bf16 [num_pages, page_size, num_kv_heads, head_dim]
+                               * ([num_pages, page_size, 2, ...] with
+                               * DSA_FLAG_KV_INTERLEAVED)                          */
+  const void *v_cache;        /* bf16, same shape as k_cache (k_cache + one K row
+                               * with DSA_FLAG_KV_INTERLEAVED)                     */
   void *out;                  /* bf16 [max_rows, num_q_heads, head_dim] (output)   */
   float *lse;                 /* fp32 [max_rows, num_q_heads] (output), nullable   */
 } dsa_step_args_t;
@@ -167,7 +170,8 @@ typedef struct {
 dsa_status_t dsa_validate_config(const dsa_config_t *cfg);
 
 /* Size and layout of the workspace dsa_step needs.  Host only.
- * The individual kernel calls use only its status word. */
+ * The individual kernel calls use its status word, and with
+ * DSA_FLAG_TOPK_HISTOGRAM dsa_indexer_scores / dsa_topk its key histogram. */
 dsa_status_t dsa_workspace_size(const dsa_config_t *cfg, size_t *bytes);
 dsa_status_t dsa_workspace_layout(const dsa_config_t *cfg, dsa_workspace_layout_t *layout);
 
@@ -218,7 +222,8 @@ dsa_status_t dsa_build_rows(const dsa_config_t *cfg, int32_t num_reqs,
  * bf16).  Products are exact, sums are fp32.  Rows are processed per score
  * block (block_first / block_nrows): all rows of a block share each key
  * tile.  scores[r, t] for t >= row_len[r] is neither read nor written.
- * scores: device fp32 [max_rows, score_width].  workspace: status word.
+ * scores: device fp32 [max_rows, score_width].  workspace: status word, and
+ * with DSA_FLAG_TOPK_HISTOGRAM the per-row key histogram it adds to.
  */
 dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, const float *w,
                                 const void *idx_cache, const float *idx_scale,
@@ -234,7 +239,9 @@ dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, cons
  * NaN below every number (-inf included).  If topk >= row_len every
  * position is selected.  Output is ascending, padded with -1.
  * scores: device fp32 [max_rows, score_width]; topk_idx: device int32
- * [max_rows, topk].  Bit-exact and deterministic.
+ * [max_rows, topk].  Bit-exact and deterministic.  With
+ * DSA_FLAG_TOPK_HISTOGRAM it starts from the workspace histogram the
+ * indexer counted (checked against the row, see the flag) and zeroes it.
  */
 dsa_status_t dsa_topk(const dsa_config_t *cfg, const float *scores, const int32_t *row_len,
                       int32_t *topk_idx, void *workspace, dsa_stream_t stream);
@@ -246,9 +253,11 @@ dsa_status_t dsa_topk(const dsa_config_t *cfg, const float *scores, const int32_
  * n = min(topk, row_len[r]), split s covers top-k slots [s*n/S, (s+1)*n/S)
  * (integer division).  A slot holding -1 is skipped; a slot holding a
  * position outside [0, row_len) sets DSA_DEV_BAD_INDEX and is skipped.  Each
- * selected K and V row is read once for the whole group.  x = sm_scale * q[r,h] . K[t,g]; the split's partial state
- * is m = max x, l = sum e^(x-m), acc = sum e^(x-m) V[t,g], probabilities in
- * fp32.  An empty split writes m = -inf, l = 0, acc = 0.
+ * selected K and V row is read once for the whole group.  With
+ * x = sm_scale * q[r,h] . K[t,g], the split's partial state is m = max x,
+ * l = sum e^(x-m), acc = sum e^(x-m) V[t,g], probabilities in fp32.  An
+ * empty split writes m = -inf, l = 0, acc = 0.  With DSA_FLAG_KV_INTERLEAVED
+ * k_cache is the one interleaved cache and v_cache = k_cache + one K row.
  * part_m, part_l: device fp32 [max_rows, num_q_heads, num_splits];
  * part_acc: device fp32 [max_rows, num_q_heads, num_splits, head_dim].
  */
@@ -271,9 +280,12 @@ dsa_status_t dsa_merge(const dsa_config_t *cfg, const float *part_m, const float
 
 /*
  * dsa_step -- indexer -> top-k -> sparse attention -> merge on `stream`,
- * with the intermediates in `workspace` (see dsa_workspace_layout).  The
- * whole step is capturable into one CUDA graph: no host sync, allocation
- * or host read, static grids.
+ * with the intermediates in `workspace` (see dsa_workspace_layout); the
+ * indexer always hands its key histogram to the top-k (as with
+ * DSA_FLAG_TOPK_HISTOGRAM).  The kernels launch with programmatic
+ * dependent launch, so each one's start overlaps its predecessor's tail.
+ * The whole step is capturable into one CUDA graph: no host sync,
+ * allocation or host read, static grids.
  */
 dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *args, void *workspace,
                       dsa_stream_t stream);
@@ -285,7 +297,8 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *args, void
  * and C hosts without a device allocator.  The page has no counterpart for
  * this entry point; it exists for those callers.
  *
- * The step's intermediates (status word, scores, top-k, split partials) go
+ * The step's intermediates (status word, scores, top-k, split partials,
+ * key histogram) go
  * to a 32 MiB array inside the library's device image instead of a caller
  * workspace; every GPU that loads the library holds those 32 MiB until the
  * process exits.  Configs whose dsa_workspace_size exceeds 32 MiB are
