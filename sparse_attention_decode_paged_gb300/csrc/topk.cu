@@ -162,14 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   const uint4 *keys4 = reinterpret_cast<const uint4 *>(keys_s);
   cg::cluster_group cl = cg::this_cluster();
   pdl_launch_dependents();
-  pdl_wait();  // the scores come from the indexer kernel
   const int C = static_cast<int>(cl.num_blocks());
   const int q = static_cast<int>(cl.block_rank());
   const int r = blockIdx.x / C;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.topk;
   int32_t *out = p.topk_idx + static_cast<size_t>(r) * K;
-  int L = p.row_len[r];
+  int L = p.row_len[r];  // row metadata, not the indexer's output: read while it finishes
+  pdl_wait();            // the scores come from the indexer kernel
   if (L < 0 || L > p.score_width) {
     if (tid == 0 && q == 0) flag_status(p.status, DSA_DEV_BAD_ROW);
     L = 0;
