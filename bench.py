@@ -77,6 +77,8 @@ def parse_args():
     ap.add_argument("--splits", type=int, default=None, help="override the top-k split count")
     ap.add_argument("--kv-layout", choices=["interleaved", "separate"], default="interleaved",
                     help="K/V cache layout: one [pages, P, 2, Hkv, D] cache (default) or two [pages, P, Hkv, D]")
+    ap.add_argument("--score-buffer-bytes", type=int, default=0,
+                    help="score-buffer budget: the indexer and top-k run in row windows that fit it (0: one window)")
     ap.add_argument("--batch", type=int, default=None,
                     help="fewer decode requests (profiling captures only; the bench line uses the full batch)")
     ap.add_argument("--e2e-steps", type=int, default=30)
@@ -91,6 +93,13 @@ def parse_args():
 # ----------------------------------------------------------------------------
 # workload description and algorithmic bytes
 # ----------------------------------------------------------------------------
+def score_windows_note(cfg) -> str:
+    from sparse_attention_decode_paged_gb300 import dsa
+    wr, nw = dsa.dsa_score_windows(cfg)
+    return (f"score buffer budget {cfg.score_buffer_bytes} B: indexer and top-k over {nw} row windows of "
+            f"{wr} rows ({wr * cfg.score_width * 4 / 2**20:.1f} MiB of scores)")
+
+
 def describe(wl, cfg, step_bytes, flush=False) -> dict:
     kd = "fp8 e4m3 + fp32 per-token scale" if wl.idx_key_dtype else "bf16"
     return {
@@ -101,6 +110,7 @@ def describe(wl, cfg, step_bytes, flush=False) -> dict:
         "page_size": int(wl.page_size), "num_splits": int(cfg.num_splits),
         "kv_layout": ("interleaved: one cache [pages, P, 2, Hkv, D], a token's K row then its V row"
                       if cfg.flags & 2 else "separate K and V caches [pages, P, Hkv, D]"),
+        **({"score_windows": score_windows_note(cfg)} if cfg.score_buffer_bytes else {}),
         "l2": f"inputs larger than L2: each step streams {step_bytes / 2**20:.0f} MiB of index keys and K/V "
               f"({step_bytes / 129e6:.1f}x the 129 MB L2)"
               + ("; plus a 256 MiB L2 flush between steps" if flush else ""),
@@ -365,39 +375,53 @@ def run_dsa(args):
     override["flags"] = dsa.DSA_FLAG_TOPK_HISTOGRAM
     if args.kv_layout == "interleaved":  # a token's K and V rows adjacent: one copy per selected token
         override["flags"] |= dsa.DSA_FLAG_KV_INTERLEAVED
+    if args.score_buffer_bytes:
+        override["score_buffer_bytes"] = args.score_buffer_bytes
     dev = DeviceStep(inp, **override)
     cfg, t, v = dev.cfg, dev.t, dev.views
     gen_s = time.time() - t_gen
     nbytes = algorithmic_bytes(wl, dev.rows)
 
     stream = torch.cuda.Stream()
+    # the launches dsa_step makes: indexer and top-k once per score window
+    # (one window without a budget), then the attention and the merge
+    wr, nw = dsa.dsa_score_windows(cfg)
+    launches = []
+    for lo in range(0, cfg.max_rows, wr):
+        win = None if nw == 1 else (lo, min(lo + wr, cfg.max_rows))
+        launches.append(("indexer", lambda s, win=win: dsa.dsa_indexer_scores(
+            cfg, t["q_idx"], t["w"], t["idx_cache"], t["idx_scale"], t["page_table"], t["row_req"],
+            t["row_len"], t["block_first"], t["block_nrows"], v["scores"], dev.workspace, s, window=win)))
+        launches.append(("topk", lambda s, win=win: dsa.dsa_topk(
+            cfg, v["scores"], t["row_len"], v["topk_idx"], dev.workspace, s, window=win)))
+    launches.append(("sparse_attn", lambda s: dsa.dsa_sparse_attn(
+        cfg, t["q"], t["k_cache"], t["v_cache"], t["page_table"], t["row_req"], t["row_len"], v["topk_idx"],
+        v["part_m"], v["part_l"], v["part_acc"], dev.workspace, s)))
+    launches.append(("merge", lambda s: dsa.dsa_merge(
+        cfg, v["part_m"], v["part_l"], v["part_acc"], t["out"], t["lse"], s)))
+    names = ["indexer", "topk", "sparse_attn", "merge"]
+    nev = len(launches) + 1
     try:
-        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nev)]
         events_in_graph = True
     except TypeError:
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
         events_in_graph = False
 
     def kernels(s, record):
-        # the four launches dsa_step makes, with event nodes between them
+        # dsa_step's launches, with event nodes between them
         if record:
             ev[0].record(s)
-        dsa.dsa_indexer_scores(cfg, t["q_idx"], t["w"], t["idx_cache"], t["idx_scale"], t["page_table"],
-                               t["row_req"], t["row_len"], t["block_first"], t["block_nrows"],
-                               v["scores"], dev.workspace, s)
-        if record:
-            ev[1].record(s)
-        dsa.dsa_topk(cfg, v["scores"], t["row_len"], v["topk_idx"], dev.workspace, s)
-        if record:
-            ev[2].record(s)
-        dsa.dsa_sparse_attn(cfg, t["q"], t["k_cache"], t["v_cache"], t["page_table"], t["row_req"],
-                            t["row_len"], v["topk_idx"], v["part_m"], v["part_l"], v["part_acc"],
-                            dev.workspace, s)
-        if record:
-            ev[3].record(s)
-        dsa.dsa_merge(cfg, v["part_m"], v["part_l"], v["part_acc"], t["out"], t["lse"], s)
-        if record:
-            ev[4].record(s)
+        for i, (_, fn) in enumerate(launches):
+            fn(s)
+            if record:
+                ev[i + 1].record(s)
+
+    def add_kernel_times(per_kernel):
+        # each kernel's time summed over its launches (one per window)
+        for n in names:
+            per_kernel[names.index(n)].append(
+                sum(ev[i].elapsed_time(ev[i + 1]) for i, (m, _) in enumerate(launches) if m == n))
 
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
@@ -466,8 +490,7 @@ def run_dsa(args):
                 step_ev[1].record(stream)
                 stream.synchronize()
                 per_inst.append(step_ev[0].elapsed_time(step_ev[1]))
-                for i in range(4):
-                    per_kernel[i].append(ev[i].elapsed_time(ev[i + 1]))
+                add_kernel_times(per_kernel)
         torch.cuda.synchronize()
         sampler.mark(False)
         if world > 1:
@@ -481,15 +504,13 @@ def run_dsa(args):
                     flush.fill_(k & 0xFF)
                 kernels(stream, record=True)
                 stream.synchronize()
-                for i in range(4):
-                    per_kernel[i].append(ev[i].elapsed_time(ev[i + 1]))
+                add_kernel_times(per_kernel)
 
     # with --flush the flush writes sit between the replays, so the step is
     # timed one replay at a time (events around the replay only)
     ms_step = statistics.mean(per_step) if args.flush else ms_back_to_back
     ms_max = max_over_ranks(ms_step, world)
 
-    names = ["indexer", "topk", "sparse_attn", "merge"]
     k_ms = {n: statistics.mean(x) for n, x in zip(names, per_kernel)}
     dominant = max(("indexer", "sparse_attn"), key=lambda n: k_ms[n])
     peak, peak_kind = measured_peaks()
@@ -532,7 +553,7 @@ def run_dsa(args):
         "rows_per_s": job["rows_per_s"],
         "hbm_gbs_step": step_gbs, "step_roofline_frac": step_gbs / peak,
         "roofline": roofline, "kernels": kernel_table, "read_probe": probe, "cpu_baseline": cpu, "e2e": e2e,
-        "clocks": clocks, "gpu_launches": 4 * args.steps, "device_status": status,
+        "clocks": clocks, "gpu_launches": (2 * nw + 2) * args.steps, "device_status": status,
         "isolated_step_us": {"median": statistics.median(per_step) * 1e3, "min": min(per_step) * 1e3,
                              "note": "one replay per synchronize, graph launch latency included"},
         "wall_s": wall_s, "setup_s": gen_s,

@@ -11,6 +11,7 @@
  *      programs and merged flash-decoding style;
  *   2  every query token is a row (request, causal length); score blocks;
  *      static padded buffers, no host syncs, CUDA-graph capture;
+ *   3  scores and selection in row windows under a score-buffer byte budget;
  *   6  exact chunk merging for long contexts;
  *   8  probabilities enter the value reduction in fp32;
  *  10  a position inside the row's length outranks padding even when its
@@ -87,7 +88,8 @@ typedef enum { DSA_KEY_BF16 = 0, DSA_KEY_FP8_E4M3 = 1 } dsa_key_dtype_t;
  *   1 <= idx_heads <= 64, idx_dim in {32, 64, 128};
  *   page_size in {16, 32, 64, 128}; 1 <= block_rows <= 4;
  *   1 <= topk <= score_width <= min(262144, max_pages_per_req * page_size);
- *   1 <= num_splits <= 64; sm_scale > 0 and finite.
+ *   1 <= num_splits <= 64; sm_scale > 0 and finite;
+ *   score_buffer_bytes == 0 or >= score_width * 4 (one score row).
  */
 typedef struct {
   int32_t num_q_heads;       /* Hq: attention query heads                        */
@@ -107,6 +109,10 @@ typedef struct {
   int32_t idx_key_dtype;     /* dsa_key_dtype_t                                    */
   float sm_scale;            /* softmax scale on q.k                              */
   int32_t flags;             /* DSA_FLAG_* bits, 0 for none                       */
+  int64_t score_buffer_bytes;/* byte budget of dsa_step's score buffer: the step
+                              * scores and selects its rows in windows of
+                              * floor(budget / (score_width * 4)) rows (commit
+                              * message 3); 0 = all max_rows rows at once   */
 } dsa_config_t;
 
 /* Bits of dsa_config_t.flags. */
@@ -115,8 +121,9 @@ enum {
    * order-preserving key into the workspace histogram, and dsa_topk uses
    * (then zeroes) those counts instead of recounting.  With this bit set,
    * every dsa_indexer_scores call must be followed by dsa_topk on the same
-   * scores and workspace before the next dsa_indexer_scores call.  dsa_step
-   * always works this way.  dsa_topk checks the hand-over: a row whose
+   * scores and workspace before the next dsa_indexer_scores call (for the
+   * _window calls: the top-k of the same window before an indexer call
+   * that covers any of its rows again).  dsa_step always works this way.  dsa_topk checks the hand-over: a row whose
    * histogram does not count exactly row_len scores (the indexer ran without
    * the bit, or twice) is recounted from its scores, with the same result; a
    * histogram with the right total that does not match the scores (the scores
@@ -157,7 +164,7 @@ typedef struct {
 /* Byte offsets of the intermediates inside a step workspace. */
 typedef struct {
   size_t status;    /* uint32 sticky device status word                   */
-  size_t scores;    /* fp32 [max_rows, score_width]                       */
+  size_t scores;    /* fp32 [window_rows, score_width] (dsa_score_windows) */
   size_t topk_idx;  /* int32 [max_rows, topk]                             */
   size_t part_m;    /* fp32 [max_rows, num_q_heads, num_splits]           */
   size_t part_l;    /* fp32 [max_rows, num_q_heads, num_splits]           */
@@ -174,6 +181,18 @@ dsa_status_t dsa_validate_config(const dsa_config_t *cfg);
  * DSA_FLAG_TOPK_HISTOGRAM dsa_indexer_scores / dsa_topk its key histogram. */
 dsa_status_t dsa_workspace_size(const dsa_config_t *cfg, size_t *bytes);
 dsa_status_t dsa_workspace_layout(const dsa_config_t *cfg, dsa_workspace_layout_t *layout);
+
+/*
+ * dsa_score_windows -- the row windows dsa_step scores and selects in
+ * (commit message 3: a score buffer under a byte budget; the window count
+ * depends only on the padded rows and the width, so a captured graph
+ * replays it).  Host only.
+ * *window_rows = max_rows if score_buffer_bytes == 0, else
+ * min(max_rows, floor(score_buffer_bytes / (score_width * 4)));
+ * *num_windows = ceil(max_rows / *window_rows).  Window i covers rows
+ * [i * window_rows, min((i + 1) * window_rows, max_rows)).
+ */
+dsa_status_t dsa_score_windows(const dsa_config_t *cfg, int32_t *window_rows, int32_t *num_windows);
 
 /* Clears the device status word (an async 4-byte memset on `stream`).
  * Call once after allocating a workspace and after reading a failure. */
@@ -233,6 +252,23 @@ dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, cons
                                 dsa_stream_t stream);
 
 /*
+ * dsa_indexer_scores_window -- dsa_indexer_scores for the rows in
+ * [row_begin, row_end) only (commit message 3).  A score block that
+ * straddles a window edge contributes its rows inside the window; the
+ * block's validity is still checked over all its rows.  Row r's scores go
+ * to scores[(r - row_begin) * score_width + t]: scores is device fp32
+ * [row_end - row_begin, score_width].  Same arithmetic, so every row's
+ * scores equal those of the whole-batch call.
+ * 0 <= row_begin < row_end <= max_rows, else DSA_ERR_INVALID_ARG.
+ */
+dsa_status_t dsa_indexer_scores_window(const dsa_config_t *cfg, int32_t row_begin, int32_t row_end,
+                                       const void *q_idx, const float *w, const void *idx_cache,
+                                       const float *idx_scale, const int32_t *page_table,
+                                       const int32_t *row_req, const int32_t *row_len,
+                                       const int32_t *block_first, const int32_t *block_nrows,
+                                       float *scores, void *workspace, dsa_stream_t stream);
+
+/*
  * dsa_topk -- length-aware exact top-k per row (commit messages 1, 10).
  * For each row, the positions of the topk largest scores[r, t] among
  * t < row_len[r]: higher score first, equal scores to the lower position,
@@ -245,6 +281,18 @@ dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, cons
  */
 dsa_status_t dsa_topk(const dsa_config_t *cfg, const float *scores, const int32_t *row_len,
                       int32_t *topk_idx, void *workspace, dsa_stream_t stream);
+
+/*
+ * dsa_topk_window -- dsa_topk for the rows in [row_begin, row_end) only
+ * (commit message 3), reading the window's scores as
+ * dsa_indexer_scores_window wrote them (scores: device fp32
+ * [row_end - row_begin, score_width]).  topk_idx is the whole device int32
+ * [max_rows, topk] array; only the window's rows are written.
+ * 0 <= row_begin < row_end <= max_rows, else DSA_ERR_INVALID_ARG.
+ */
+dsa_status_t dsa_topk_window(const dsa_config_t *cfg, int32_t row_begin, int32_t row_end,
+                             const float *scores, const int32_t *row_len, int32_t *topk_idx,
+                             void *workspace, dsa_stream_t stream);
 
 /*
  * dsa_sparse_attn -- sparse GQA attention over the selected keys, split
@@ -282,7 +330,11 @@ dsa_status_t dsa_merge(const dsa_config_t *cfg, const float *part_m, const float
  * dsa_step -- indexer -> top-k -> sparse attention -> merge on `stream`,
  * with the intermediates in `workspace` (see dsa_workspace_layout); the
  * indexer always hands its key histogram to the top-k (as with
- * DSA_FLAG_TOPK_HISTOGRAM).  The kernels launch with programmatic
+ * DSA_FLAG_TOPK_HISTOGRAM).  With a score_buffer_bytes budget the indexer
+ * and the top-k run once per row window (dsa_score_windows) on one score
+ * buffer of window_rows rows, each window's indexer starting after the
+ * previous window's top-k has finished; the results equal those of one
+ * window.  The top-k, attention and merge launch with programmatic
  * dependent launch, so each one's start overlaps its predecessor's tail.
  * The whole step is capturable into one CUDA graph: no host sync,
  * allocation or host read, static grids.

@@ -59,6 +59,14 @@ dsa_status_t cuda_status(cudaError_t e, const char *what) {
   return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Rows per score window (commit message 3): all rows without a budget, else
+// as many whole score rows as the budget holds.  The config is validated.
+int32_t window_rows_of(const dsa_config_t *c) {
+  if (c->score_buffer_bytes == 0) return c->max_rows;
+  const long long fit = c->score_buffer_bytes / (static_cast<long long>(c->score_width) * 4);
+  return static_cast<int32_t>(std::min<long long>(fit, c->max_rows));
+}
+
 dsa_status_t layout_of(const dsa_config_t *c, dsa_workspace_layout_t *l) {
   const size_t R = static_cast<size_t>(c->max_rows);
   const size_t HS = static_cast<size_t>(c->num_q_heads) * c->num_splits;
@@ -66,7 +74,7 @@ dsa_status_t layout_of(const dsa_config_t *c, dsa_workspace_layout_t *l) {
   l->status = off;
   off += 256;
   l->scores = off;
-  off = align256(off + R * c->score_width * sizeof(float));
+  off = align256(off + static_cast<size_t>(window_rows_of(c)) * c->score_width * sizeof(float));
   l->topk_idx = off;
   off = align256(off + R * c->topk * sizeof(int32_t));
   l->part_m = off;
@@ -139,6 +147,19 @@ dsa_status_t dsa_validate_config(const dsa_config_t *c) {
   if (static_cast<long long>(c->max_reqs) * c->max_pages_per_req > 0x7FFFFFFFLL)
     return fail(DSA_ERR_INVALID_ARG, "page table larger than 2^31 entries");
   if (c->max_rows > 4096) return fail(DSA_ERR_UNSUPPORTED, "max_rows %d > 4096", c->max_rows);
+  if (c->score_buffer_bytes < 0 ||
+      (c->score_buffer_bytes > 0 && c->score_buffer_bytes < static_cast<long long>(c->score_width) * 4))
+    return fail(DSA_ERR_INVALID_ARG, "score_buffer_bytes %lld must be 0 or hold one score row (%lld bytes)",
+                static_cast<long long>(c->score_buffer_bytes), static_cast<long long>(c->score_width) * 4);
+  return ok();
+}
+
+dsa_status_t dsa_score_windows(const dsa_config_t *cfg, int32_t *window_rows, int32_t *num_windows) {
+  DSA_CHECK_CFG(cfg);
+  if (window_rows == nullptr || num_windows == nullptr) return fail(DSA_ERR_INVALID_ARG, "output is NULL");
+  const int32_t wr = window_rows_of(cfg);
+  *window_rows = wr;
+  *num_windows = (cfg->max_rows + wr - 1) / wr;
   return ok();
 }
 
@@ -238,12 +259,21 @@ uint32_t *key_hist_of(const dsa_config_t *cfg, void *workspace) {
   return reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + l.key_hist);
 }
 
-dsa_status_t indexer_impl(const dsa_config_t *cfg, const void *q_idx, const float *w,
+dsa_status_t check_window(const dsa_config_t *cfg, int32_t row_begin, int32_t row_end) {
+  if (row_begin < 0 || row_end > cfg->max_rows || row_begin >= row_end)
+    return fail(DSA_ERR_INVALID_ARG, "row window [%d, %d) not inside [0, %d)", row_begin, row_end,
+                cfg->max_rows);
+  return DSA_OK;
+}
+
+dsa_status_t indexer_impl(const dsa_config_t *cfg, int32_t row_begin, int32_t row_end,
+                          const void *q_idx, const float *w,
                           const void *idx_cache, const float *idx_scale, const int32_t *page_table,
                           const int32_t *row_req, const int32_t *row_len, const int32_t *block_first,
                           const int32_t *block_nrows, float *scores, void *workspace, bool hist,
                           dsa_stream_t stream) {
   DSA_CHECK_CFG(cfg);
+  if (check_window(cfg, row_begin, row_end) != DSA_OK) return DSA_ERR_INVALID_ARG;
   DSA_CHECK_DEV_PTR(q_idx);
   DSA_CHECK_DEV_PTR(w);
   DSA_CHECK_DEV_PTR(idx_cache);
@@ -277,12 +307,16 @@ dsa_status_t indexer_impl(const dsa_config_t *cfg, const void *q_idx, const floa
   p.page_size = cfg->page_size;
   p.block_rows = cfg->block_rows;
   p.row_hist = hist ? key_hist_of(cfg, workspace) : nullptr;
+  p.row_lo = row_begin;
+  p.row_hi = row_end;
   return cuda_status(dsa::launch_indexer_tc(*cfg, p, stream), "indexer launch");
 }
 
-dsa_status_t topk_impl(const dsa_config_t *cfg, const float *scores, const int32_t *row_len,
-                       int32_t *topk_idx, void *workspace, bool hist, dsa_stream_t stream) {
+dsa_status_t topk_impl(const dsa_config_t *cfg, int32_t row_begin, int32_t row_end, const float *scores,
+                       const int32_t *row_len, int32_t *topk_idx, void *workspace, bool hist,
+                       dsa_stream_t stream) {
   DSA_CHECK_CFG(cfg);
+  if (check_window(cfg, row_begin, row_end) != DSA_OK) return DSA_ERR_INVALID_ARG;
   DSA_CHECK_DEV_PTR(scores);
   DSA_CHECK_DEV_PTR(row_len);
   DSA_CHECK_DEV_PTR(topk_idx);
@@ -295,7 +329,8 @@ dsa_status_t topk_impl(const dsa_config_t *cfg, const float *scores, const int32
   p.row_hist = hist ? key_hist_of(cfg, workspace) : nullptr;
   p.topk = cfg->topk;
   p.score_width = cfg->score_width;
-  return cuda_status(dsa::launch_topk(*cfg, p, stream), "top-k launch");
+  p.row_lo = row_begin;
+  return cuda_status(dsa::launch_topk(*cfg, p, row_end - row_begin, stream), "top-k launch");
 }
 }  // namespace
 
@@ -308,14 +343,33 @@ dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, cons
                                 const int32_t *block_nrows, float *scores, void *workspace,
                                 dsa_stream_t stream) {
   const bool hist = cfg != nullptr && (cfg->flags & DSA_FLAG_TOPK_HISTOGRAM) != 0;
-  return indexer_impl(cfg, q_idx, w, idx_cache, idx_scale, page_table, row_req, row_len, block_first,
-                      block_nrows, scores, workspace, hist, stream);
+  return indexer_impl(cfg, 0, cfg != nullptr ? cfg->max_rows : 0, q_idx, w, idx_cache, idx_scale, page_table,
+                      row_req, row_len, block_first, block_nrows, scores, workspace, hist, stream);
+}
+
+dsa_status_t dsa_indexer_scores_window(const dsa_config_t *cfg, int32_t row_begin, int32_t row_end,
+                                       const void *q_idx, const float *w, const void *idx_cache,
+                                       const float *idx_scale, const int32_t *page_table,
+                                       const int32_t *row_req, const int32_t *row_len,
+                                       const int32_t *block_first, const int32_t *block_nrows,
+                                       float *scores, void *workspace, dsa_stream_t stream) {
+  const bool hist = cfg != nullptr && (cfg->flags & DSA_FLAG_TOPK_HISTOGRAM) != 0;
+  return indexer_impl(cfg, row_begin, row_end, q_idx, w, idx_cache, idx_scale, page_table, row_req, row_len,
+                      block_first, block_nrows, scores, workspace, hist, stream);
 }
 
 dsa_status_t dsa_topk(const dsa_config_t *cfg, const float *scores, const int32_t *row_len,
                       int32_t *topk_idx, void *workspace, dsa_stream_t stream) {
   const bool hist = cfg != nullptr && (cfg->flags & DSA_FLAG_TOPK_HISTOGRAM) != 0;
-  return topk_impl(cfg, scores, row_len, topk_idx, workspace, hist, stream);
+  return topk_impl(cfg, 0, cfg != nullptr ? cfg->max_rows : 0, scores, row_len, topk_idx, workspace, hist,
+                   stream);
+}
+
+dsa_status_t dsa_topk_window(const dsa_config_t *cfg, int32_t row_begin, int32_t row_end,
+                             const float *scores, const int32_t *row_len, int32_t *topk_idx,
+                             void *workspace, dsa_stream_t stream) {
+  const bool hist = cfg != nullptr && (cfg->flags & DSA_FLAG_TOPK_HISTOGRAM) != 0;
+  return topk_impl(cfg, row_begin, row_end, scores, row_len, topk_idx, workspace, hist, stream);
 }
 
 dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void *k_cache,
@@ -402,13 +456,20 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *a, void *w
   float *part_m = reinterpret_cast<float *>(ws + l.part_m);
   float *part_l = reinterpret_cast<float *>(ws + l.part_l);
   float *part_acc = reinterpret_cast<float *>(ws + l.part_acc);
-  // the indexer counts the first-level key histogram the top-k then uses
-  dsa_status_t st = indexer_impl(cfg, a->q_idx, a->w, a->idx_cache, a->idx_scale, a->page_table,
-                                 a->row_req, a->row_len, a->block_first, a->block_nrows, scores,
-                                 workspace, true, stream);
-  if (st != DSA_OK) return st;
-  st = topk_impl(cfg, scores, a->row_len, topk_idx, workspace, true, stream);
-  if (st != DSA_OK) return st;
+  // per row window (one window without a score budget): the indexer counts
+  // the first-level key histogram the top-k then uses; the next window's
+  // indexer is an ordinary launch, so it starts once this top-k is done
+  // reading the shared score buffer
+  const int32_t wr = window_rows_of(cfg);
+  dsa_status_t st = DSA_OK;
+  for (int32_t lo = 0; lo < cfg->max_rows; lo += wr) {
+    const int32_t hi = std::min(lo + wr, cfg->max_rows);
+    st = indexer_impl(cfg, lo, hi, a->q_idx, a->w, a->idx_cache, a->idx_scale, a->page_table, a->row_req,
+                      a->row_len, a->block_first, a->block_nrows, scores, workspace, true, stream);
+    if (st != DSA_OK) return st;
+    st = topk_impl(cfg, lo, hi, scores, a->row_len, topk_idx, workspace, true, stream);
+    if (st != DSA_OK) return st;
+  }
   st = dsa_sparse_attn(cfg, a->q, a->k_cache, a->v_cache, a->page_table, a->row_req, a->row_len,
                        topk_idx, part_m, part_l, part_acc, workspace, stream);
   if (st != DSA_OK) return st;

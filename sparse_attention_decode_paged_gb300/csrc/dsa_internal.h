@@ -18,20 +18,22 @@ struct IndexerParams {
   const int32_t *row_len;
   const int32_t *block_first;
   const int32_t *block_nrows;
-  float *scores;            // [R, W]
+  float *scores;            // [row_hi - row_lo, W]: row r at (r - row_lo) * W
   uint32_t *status;
   uint32_t *row_hist;       // [R, 4096] key-bin counts for the top-k, or null
   int32_t idx_heads, idx_dim, max_rows, max_reqs, max_pages_per_req, score_width, num_pages;
   int32_t page_size, block_rows;
+  int32_t row_lo, row_hi;   // the row window scored (0, max_rows for all rows)
 };
 
 struct TopkParams {
-  const float *scores;
+  const float *scores;     // [rows of the window, W]
   const int32_t *row_len;
   int32_t *topk_idx;
   uint32_t *status;
   uint32_t *row_hist;  // [R, 4096] filled by the indexer (used, then zeroed), or null
   int32_t topk, score_width;
+  int32_t row_lo;          // first row of the window; one cluster per row of it
 };
 
 struct AttnParams {
@@ -93,7 +95,7 @@ dsa_status_t set_error(dsa_status_t st, const char *fmt, ...);
 
 // Each launcher returns the launch error (cudaSuccess when queued).
 cudaError_t launch_indexer_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStream_t st);
-cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, cudaStream_t st);
+cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, int rows, cudaStream_t st);
 cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cudaStream_t st);
 cudaError_t launch_merge(const dsa_config_t &cfg, const MergeParams &p, cudaStream_t st);
 

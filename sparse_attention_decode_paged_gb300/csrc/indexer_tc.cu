@@ -90,10 +90,12 @@ struct BlockInfo {
   int lens[4];
 };
 
+// A block's rows inside the scored window (a block may straddle its edge).
 __device__ __forceinline__ BlockInfo load_block(const IndexerParams &p, int b) {
   BlockInfo bi;
-  bi.first = p.block_first[b];
-  bi.nrows = p.block_nrows[b];
+  const int first = p.block_first[b];
+  bi.first = max(first, p.row_lo);
+  bi.nrows = min(first + p.block_nrows[b], p.row_hi) - bi.first;
   bi.req = p.row_req[bi.first];
   bi.lmax = 0;
 #pragma unroll
@@ -282,15 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int req = ok ? p.row_req[first] : 0;
       ok = ok && req >= 0 && req < p.max_reqs;
       int lmax = 0;
-      for (int i = 0; i < nrows && ok; ++i) {
+      for (int i = 0; i < nrows && ok; ++i) {  // checked over the whole block
         const int L = p.row_len[first + i];
         if (p.row_req[first + i] != req || L < 0 || L > p.score_width) ok = false;
-        lmax = max(lmax, L);
+        if (first + i >= p.row_lo && first + i < p.row_hi) lmax = max(lmax, L);  // rows scored here
       }
       if (!ok) {
         if (blockIdx.x == 0) flag_status(p.status, DSA_DEV_BAD_BLOCK);
       } else {
-        nt = (lmax + kTok - 1) / kTok;
+        nt = (lmax + kTok - 1) / kTok;  // 0 for a block outside the window
       }
     }
     prefix[b + 1] = nt;
@@ -665,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < L) {
           const float score = sum * sc;
           // kept in L2 for the top-k that reads them next (the key stream is evict-first)
-          tc::st_global_hint(p.scores + static_cast<size_t>(bi.first + rr) * p.score_width + t, score, keep);
+          tc::st_global_hint(p.scores + static_cast<size_t>(bi.first + rr - p.row_lo) * p.score_width + t, score, keep);
           if (p.row_hist != nullptr)  // first-level histogram for the top-k that follows
             atomicAdd(p.row_hist + static_cast<size_t>(bi.first + rr) * kKeyBins + (order_key(score) >> 20), 1u);
         }

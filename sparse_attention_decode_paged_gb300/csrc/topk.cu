@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   pdl_launch_dependents();
   const int C = static_cast<int>(cl.num_blocks());
   const int q = static_cast<int>(cl.block_rank());
-  const int r = blockIdx.x / C;
+  const int wr = blockIdx.x / C;  // row within the window
+  const int r = p.row_lo + wr;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.topk;
   int32_t *out = p.topk_idx + static_cast<size_t>(r) * K;
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   const int lo = min(L, q * seg);
   const int n = min(L, lo + seg) - lo;
   const int ng = (n + 4 * kThreads - 1) / (4 * kThreads);  // <= NG
-  const float *srow = p.scores + static_cast<size_t>(r) * p.score_width + lo;
+  const float *srow = p.scores + static_cast<size_t>(wr) * p.score_width + lo;
 
   // ---- A. the row's histogram and this segment's keys
   uint32_t gh[kBins1 / kThreads];
@@ -466,8 +467,8 @@ int topk_cluster_size(int score_width, int max_rows) {
   return c;
 }
 
-cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, cudaStream_t st) {
-  const int C = topk_cluster_size(cfg.score_width, cfg.max_rows);
+cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, int rows, cudaStream_t st) {
+  const int C = topk_cluster_size(cfg.score_width, rows);
   const int seg_w = (((cfg.score_width + C - 1) / C) + 127) & ~127;
   if (seg_w > kSegMax) return cudaErrorInvalidValue;
   const int groups = (seg_w + 4 * kThreads - 1) / (4 * kThreads);
@@ -477,7 +478,7 @@ cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, cudaStream
            : ng == 4 ? topk_cluster_kernel<4> : topk_cluster_kernel<8>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  e = launch_pdl(k, dim3(static_cast<unsigned>(cfg.max_rows * C)), dim3(kThreads), smem, st,
+  e = launch_pdl(k, dim3(static_cast<unsigned>(rows * C)), dim3(kThreads), smem, st,
                  static_cast<unsigned>(C), p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

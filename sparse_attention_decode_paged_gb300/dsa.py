@@ -40,8 +40,9 @@ DSA_FLAG_KV_INTERLEAVED = 1 << 1
 
 EXPORTED = (
     "dsa_validate_config", "dsa_workspace_size", "dsa_workspace_layout",
-    "dsa_reset_device_status", "dsa_read_device_status", "dsa_build_rows",
-    "dsa_indexer_scores", "dsa_topk", "dsa_sparse_attn", "dsa_merge", "dsa_step",
+    "dsa_reset_device_status", "dsa_read_device_status", "dsa_build_rows", "dsa_score_windows",
+    "dsa_indexer_scores", "dsa_indexer_scores_window", "dsa_topk", "dsa_topk_window",
+    "dsa_sparse_attn", "dsa_merge", "dsa_step",
     "dsa_step_noalloc", "dsa_last_error", "dsa_version",
 )
 
@@ -57,7 +58,8 @@ class dsa_config_t(ctypes.Structure):
         "num_q_heads", "num_kv_heads", "head_dim", "idx_heads", "idx_dim", "page_size",
         "topk", "num_splits", "max_rows", "max_reqs", "max_pages_per_req", "score_width",
         "num_pages", "block_rows", "idx_key_dtype")] + [("sm_scale", ctypes.c_float),
-                                                        ("flags", ctypes.c_int32)]
+                                                        ("flags", ctypes.c_int32),
+                                                        ("score_buffer_bytes", ctypes.c_int64)]
 
 
 class dsa_step_args_t(ctypes.Structure):
@@ -87,8 +89,11 @@ def _load():
         "dsa_reset_device_status": [vp, vp],
         "dsa_read_device_status": [vp, ctypes.POINTER(ctypes.c_uint32), vp],
         "dsa_build_rows": [cfgp, i32, i32p, i32p, i32p, i32p, i32p, i32p, i32p, i32p, i32p],
+        "dsa_score_windows": [cfgp, i32p, i32p],
         "dsa_indexer_scores": [cfgp] + [vp] * 12,
+        "dsa_indexer_scores_window": [cfgp, i32, i32] + [vp] * 12,
         "dsa_topk": [cfgp] + [vp] * 5,
+        "dsa_topk_window": [cfgp, i32, i32] + [vp] * 5,
         "dsa_sparse_attn": [cfgp] + [vp] * 12,
         "dsa_merge": [cfgp] + [vp] * 6,
         "dsa_step": [cfgp, ctypes.POINTER(dsa_step_args_t), vp, vp],
@@ -122,12 +127,14 @@ def version() -> str:
 # ----------------------------------------------------------------------------
 def make_config(*, num_q_heads, num_kv_heads, head_dim, idx_heads, idx_dim, page_size, topk,
                 num_splits, max_rows, max_reqs, max_pages_per_req, score_width, num_pages,
-                block_rows=1, idx_key_dtype=DSA_KEY_BF16, sm_scale=None, flags=0) -> dsa_config_t:
+                block_rows=1, idx_key_dtype=DSA_KEY_BF16, sm_scale=None, flags=0,
+                score_buffer_bytes=0) -> dsa_config_t:
     if sm_scale is None:
         sm_scale = 1.0 / float(np.sqrt(head_dim))
     return dsa_config_t(num_q_heads, num_kv_heads, head_dim, idx_heads, idx_dim, page_size, topk,
                         num_splits, max_rows, max_reqs, max_pages_per_req, score_width,
-                        num_pages, block_rows, idx_key_dtype, float(sm_scale), int(flags))
+                        num_pages, block_rows, idx_key_dtype, float(sm_scale), int(flags),
+                        int(score_buffer_bytes))
 
 
 def config_from_workload(wl, num_pages: int, **override) -> dsa_config_t:
@@ -199,9 +206,11 @@ def alloc_workspace(cfg: dsa_config_t, device=None) -> torch.Tensor:
 
 
 def workspace_views(cfg: dsa_config_t, workspace: torch.Tensor) -> dict:
-    """Typed views of the step intermediates inside a workspace."""
+    """Typed views of the step intermediates inside a workspace (the score
+    buffer holds one window of rows, all max_rows without a budget)."""
     lay = dsa_workspace_layout(cfg)
     R, W, K = cfg.max_rows, cfg.score_width, cfg.topk
+    WR = dsa_score_windows(cfg)[0]
     HS = cfg.num_q_heads * cfg.num_splits
 
     def view(off, n, dtype, shape):
@@ -210,7 +219,7 @@ def workspace_views(cfg: dsa_config_t, workspace: torch.Tensor) -> dict:
 
     return dict(
         status=view(lay["status"], 1, torch.int32, (1,)),
-        scores=view(lay["scores"], R * W, torch.float32, (R, W)),
+        scores=view(lay["scores"], WR * W, torch.float32, (WR, W)),
         topk_idx=view(lay["topk_idx"], R * K, torch.int32, (R, K)),
         part_m=view(lay["part_m"], R * HS, torch.float32, (R, cfg.num_q_heads, cfg.num_splits)),
         part_l=view(lay["part_l"], R * HS, torch.float32, (R, cfg.num_q_heads, cfg.num_splits)),
@@ -258,30 +267,50 @@ def dsa_build_rows(cfg: dsa_config_t, req_cache_len, req_new_tokens) -> dict:
     return outs
 
 
+def dsa_score_windows(cfg) -> tuple:
+    """(window_rows, num_windows) of the step's score windows."""
+    wr, nw = ctypes.c_int32(), ctypes.c_int32()
+    _check(_lib.dsa_score_windows(ctypes.byref(cfg), ctypes.byref(wr), ctypes.byref(nw)))
+    return int(wr.value), int(nw.value)
+
+
 def dsa_indexer_scores(cfg, q_idx, w, idx_cache, idx_scale, page_table, row_req, row_len,
-                       block_first, block_nrows, scores, workspace, stream=None) -> None:
+                       block_first, block_nrows, scores, workspace, stream=None, window=None) -> None:
+    """Scores of every row into scores [max_rows, score_width], or with
+    window=(row_begin, row_end) of those rows only, into scores
+    [row_end - row_begin, score_width] (dsa_indexer_scores_window)."""
     R = cfg.max_rows
     keyt = _FP8 if cfg.idx_key_dtype == DSA_KEY_FP8_E4M3 else _BF16
-    _check(_lib.dsa_indexer_scores(
-        ctypes.byref(cfg),
-        _dev(q_idx, "q_idx", _BF16, R * cfg.idx_heads * cfg.idx_dim),
-        _dev(w, "w", (torch.float32,), R * cfg.idx_heads),
-        _dev(idx_cache, "idx_cache", keyt, cfg.num_pages * cfg.page_size * cfg.idx_dim),
-        _dev(idx_scale, "idx_scale", (torch.float32,), cfg.num_pages * cfg.page_size),
-        _dev(page_table, "page_table", (torch.int32,), cfg.max_reqs * cfg.max_pages_per_req),
-        _dev(row_req, "row_req", (torch.int32,), R), _dev(row_len, "row_len", (torch.int32,), R),
-        _dev(block_first, "block_first", (torch.int32,), R),
-        _dev(block_nrows, "block_nrows", (torch.int32,), R),
-        _dev(scores, "scores", (torch.float32,), R * cfg.score_width),
-        _ws(workspace), _stream(stream)))
+    lo, hi = (0, R) if window is None else (int(window[0]), int(window[1]))
+    args = (_dev(q_idx, "q_idx", _BF16, R * cfg.idx_heads * cfg.idx_dim),
+            _dev(w, "w", (torch.float32,), R * cfg.idx_heads),
+            _dev(idx_cache, "idx_cache", keyt, cfg.num_pages * cfg.page_size * cfg.idx_dim),
+            _dev(idx_scale, "idx_scale", (torch.float32,), cfg.num_pages * cfg.page_size),
+            _dev(page_table, "page_table", (torch.int32,), cfg.max_reqs * cfg.max_pages_per_req),
+            _dev(row_req, "row_req", (torch.int32,), R), _dev(row_len, "row_len", (torch.int32,), R),
+            _dev(block_first, "block_first", (torch.int32,), R),
+            _dev(block_nrows, "block_nrows", (torch.int32,), R),
+            _dev(scores, "scores", (torch.float32,), max(hi - lo, 0) * cfg.score_width),
+            _ws(workspace), _stream(stream))
+    if window is None:
+        _check(_lib.dsa_indexer_scores(ctypes.byref(cfg), *args))
+    else:
+        _check(_lib.dsa_indexer_scores_window(ctypes.byref(cfg), lo, hi, *args))
 
 
-def dsa_topk(cfg, scores, row_len, topk_idx, workspace, stream=None) -> None:
+def dsa_topk(cfg, scores, row_len, topk_idx, workspace, stream=None, window=None) -> None:
+    """Top-k of every row from scores [max_rows, score_width], or with
+    window=(row_begin, row_end) of those rows only, from scores
+    [row_end - row_begin, score_width] (dsa_topk_window)."""
     R = cfg.max_rows
-    _check(_lib.dsa_topk(
-        ctypes.byref(cfg), _dev(scores, "scores", (torch.float32,), R * cfg.score_width),
-        _dev(row_len, "row_len", (torch.int32,), R),
-        _dev(topk_idx, "topk_idx", (torch.int32,), R * cfg.topk), _ws(workspace), _stream(stream)))
+    lo, hi = (0, R) if window is None else (int(window[0]), int(window[1]))
+    args = (_dev(scores, "scores", (torch.float32,), max(hi - lo, 0) * cfg.score_width),
+            _dev(row_len, "row_len", (torch.int32,), R),
+            _dev(topk_idx, "topk_idx", (torch.int32,), R * cfg.topk), _ws(workspace), _stream(stream))
+    if window is None:
+        _check(_lib.dsa_topk(ctypes.byref(cfg), *args))
+    else:
+        _check(_lib.dsa_topk_window(ctypes.byref(cfg), lo, hi, *args))
 
 
 def _kv_ptrs(cfg, k_cache, v_cache):
