@@ -354,7 +354,8 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *args, void
  * to a 32 MiB array inside the library's device image instead of a caller
  * workspace; every GPU that loads the library holds those 32 MiB until the
  * process exits.  Configs whose dsa_workspace_size exceeds 32 MiB are
- * rejected with DSA_ERR_CAPACITY before anything is launched.  The call
+ * rejected with DSA_ERR_CAPACITY before anything is launched (a
+ * score_buffer_bytes budget shrinks the score part of that size).  The call
  * itself allocates nothing: the first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current, so make
  * that first call outside stream capture.  All calls on a device share the
