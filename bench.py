@@ -604,39 +604,32 @@ def run_read_probe(dev, nbytes_idx, stream, reps=25):
 
 def run_e2e(args, dsa, dev, inp, stream, flush):
     """µs per step through the public API with host buffers: per step the rows
-    are built on the host (dsa_build_rows) into pinned buffers, then one CUDA
-    graph copies the step's inputs host -> device, runs dsa_step and copies
-    the output back (the way a serving loop replays a captured step), and the
-    host waits for it.  The same sequence issued eagerly is reported too."""
+    are built on the host (dsa_build_rows, straight into the pinned staging
+    copy of the device input arena), then one CUDA graph copies that arena
+    (row maps, page table, q_idx, w, q) host -> device in one copy, runs
+    dsa_step and copies the output arena (out, lse) back in one copy (the way
+    a serving loop replays a captured step), and the host waits for it.  The
+    same sequence issued eagerly is reported too."""
     import torch
-    cfg, t = dev.cfg, dev.t
-    pin = lambda x: x.cpu().pin_memory()  # noqa: E731
-    h_q_idx, h_w, h_q = pin(t["q_idx"]), pin(t["w"]), pin(t["q"])
-    h_pt = pin(t["page_table"])
-    h_rows = {k: torch.empty(cfg.max_rows, dtype=torch.int32).pin_memory()
-              for k in ("row_req", "row_len", "block_first", "block_nrows")}
-    h_out = torch.empty_like(t["out"], device="cpu").pin_memory()
-    h_lse = torch.empty_like(t["lse"], device="cpu").pin_memory()
-    h2d = (h_q_idx.numel() * 2 + h_w.numel() * 4 + h_q.numel() * 2 + h_pt.numel() * 4
-           + 4 * cfg.max_rows * 4)
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
-    cache_len, new_tokens = inp["cache_len"], inp["new_tokens"]
+    from sparse_attention_decode_paged_gb300.harness import DEVICE_ROW_KEYS
+    cfg, R = dev.cfg, dev.cfg.max_rows
+    h_in = dev.inputs.cpu().pin_memory()  # this step's inputs, staged on the host
+    h_out = torch.empty_like(dev.outputs, device="cpu").pin_memory()
+    # host views of the staged row maps (same offsets as the device arena)
+    staged = {k: h_in[dev.t[k].data_ptr() - dev.inputs.data_ptr():][:4 * R].view(torch.int32)
+              for k in DEVICE_ROW_KEYS}
+    staged["row_pos"] = torch.empty(R, dtype=torch.int32)  # not needed on the device
+    h2d, d2h = dev.inputs.numel(), dev.outputs.numel()
+    cache_len = np.ascontiguousarray(inp["cache_len"], dtype=np.int32)
+    new_tokens = np.ascontiguousarray(inp["new_tokens"], dtype=np.int32)
 
     def host_rows():
-        rows = dsa.dsa_build_rows(cfg, cache_len, new_tokens)
-        for name, h in h_rows.items():
-            h.numpy()[:] = rows[name]
+        dsa.dsa_build_rows(cfg, cache_len, new_tokens, out=staged)
 
     def device_part(s):
-        for name, h in h_rows.items():
-            t[name].copy_(h, non_blocking=True)
-        t["page_table"].copy_(h_pt, non_blocking=True)
-        t["q_idx"].copy_(h_q_idx, non_blocking=True)
-        t["w"].copy_(h_w, non_blocking=True)
-        t["q"].copy_(h_q, non_blocking=True)
+        dev.inputs.copy_(h_in, non_blocking=True)
         dsa.dsa_step(cfg, dev.args, dev.workspace, s)
-        h_out.copy_(t["out"], non_blocking=True)
-        h_lse.copy_(t["lse"], non_blocking=True)
+        h_out.copy_(dev.outputs, non_blocking=True)
 
     with torch.cuda.stream(stream):
         host_rows()
@@ -670,8 +663,9 @@ def run_e2e(args, dsa, dev, inp, stream, flush):
     return {"value": statistics.median(times) * 1e6, "unit": "us", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": len(times),
             "eager_us": statistics.median(eager) * 1e6,
-            "path": "dsa_build_rows into pinned buffers + one CUDA-graph replay of (H2D copies, dsa_step, D2H "
-                    "copies) + host wait, wall clock median; eager_us: the same calls issued eagerly"}
+            "path": "dsa_build_rows into the pinned input staging + one CUDA-graph replay of (one H2D copy of "
+                    "the input arena, dsa_step, one D2H copy of the output arena) + host wait, wall clock "
+                    "median; eager_us: the same calls issued eagerly"}
 
 
 def main():

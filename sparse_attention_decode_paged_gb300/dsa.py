@@ -88,7 +88,7 @@ def _load():
         "dsa_workspace_layout": [cfgp, ctypes.POINTER(dsa_workspace_layout_t)],
         "dsa_reset_device_status": [vp, vp],
         "dsa_read_device_status": [vp, ctypes.POINTER(ctypes.c_uint32), vp],
-        "dsa_build_rows": [cfgp, i32, i32p, i32p, i32p, i32p, i32p, i32p, i32p, i32p, i32p],
+        "dsa_build_rows": [cfgp, i32] + [vp] * 7 + [i32p, i32p],
         "dsa_score_windows": [cfgp, i32p, i32p],
         "dsa_indexer_scores": [cfgp] + [vp] * 12,
         "dsa_indexer_scores_window": [cfgp, i32, i32] + [vp] * 12,
@@ -244,23 +244,37 @@ def dsa_read_device_status(workspace, stream=None) -> int:
     return int(v.value)
 
 
-def dsa_build_rows(cfg: dsa_config_t, req_cache_len, req_new_tokens) -> dict:
-    """Host row builder.  Inputs: int sequences; outputs: numpy int32 arrays."""
-    cl = np.ascontiguousarray(np.asarray(req_cache_len, dtype=np.int32))
-    nt = np.ascontiguousarray(np.asarray(req_new_tokens, dtype=np.int32))
+_ROW_KEYS = ("row_req", "row_len", "row_pos", "block_first", "block_nrows")
+
+
+def _host_i32(a, name, n):
+    """Address of a contiguous int32 host buffer of at least n elements (a
+    numpy array, or a CPU torch tensor such as a pinned staging buffer)."""
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda or a.dtype != torch.int32 or not a.is_contiguous() or a.numel() < n:
+            raise ValueError(f"{name}: expected a contiguous CPU int32 tensor of >= {n} elements")
+        return a.data_ptr()
+    if not isinstance(a, np.ndarray) or a.dtype != np.int32 or not a.flags.c_contiguous or a.size < n:
+        raise ValueError(f"{name}: expected a contiguous int32 numpy array of >= {n} elements")
+    return a.ctypes.data
+
+
+def dsa_build_rows(cfg: dsa_config_t, req_cache_len, req_new_tokens, out=None) -> dict:
+    """Host row builder.  Inputs: int sequences.  Outputs: numpy int32 arrays
+    [max_rows] keyed row_req, row_len, row_pos, block_first, block_nrows, plus
+    num_rows and num_blocks.  With out = a dict of five such host buffers
+    (numpy arrays or CPU torch tensors, e.g. pinned staging for the copy to
+    the device) the rows are written there in place and the dict is returned
+    with the two counts added."""
+    cl = np.ascontiguousarray(req_cache_len, dtype=np.int32)
+    nt = np.ascontiguousarray(req_new_tokens, dtype=np.int32)
     if cl.shape != nt.shape or cl.ndim != 1:
         raise ValueError("req_cache_len and req_new_tokens must be 1-D and equal in length")
     R = cfg.max_rows
-    outs = {k: np.zeros(R, np.int32) for k in ("row_req", "row_len", "row_pos", "block_first", "block_nrows")}
+    outs = {k: np.zeros(R, np.int32) for k in _ROW_KEYS} if out is None else out
     nr, nb = ctypes.c_int32(0), ctypes.c_int32(0)
-    i32p = ctypes.POINTER(ctypes.c_int32)
-
-    def ptr(a):
-        return a.ctypes.data_as(i32p)
-
-    _check(_lib.dsa_build_rows(ctypes.byref(cfg), int(cl.size), ptr(cl), ptr(nt),
-                               ptr(outs["row_req"]), ptr(outs["row_len"]), ptr(outs["row_pos"]),
-                               ptr(outs["block_first"]), ptr(outs["block_nrows"]),
+    _check(_lib.dsa_build_rows(ctypes.byref(cfg), int(cl.size), cl.ctypes.data, nt.ctypes.data,
+                               *(_host_i32(outs[k], k, R) for k in _ROW_KEYS),
                                ctypes.byref(nr), ctypes.byref(nb)))
     outs["num_rows"] = int(nr.value)
     outs["num_blocks"] = int(nb.value)

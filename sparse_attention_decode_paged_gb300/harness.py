@@ -22,8 +22,28 @@ def to_device(a: np.ndarray | None, device="cuda", kind: str = "raw"):
     return t
 
 
+DEVICE_ROW_KEYS = ("row_req", "row_len", "block_first", "block_nrows")
+
+
+def _arena(parts, device):
+    """One byte buffer holding several tensors, each at a 256-byte aligned
+    offset: parts = [(name, dtype, shape)] -> (buffer, {name: view})."""
+    off, spans = 0, []
+    for name, dtype, shape in parts:
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        spans.append((name, dtype, shape, off, n))
+        off = (off + n + 255) // 256 * 256
+    buf = torch.zeros(max(off, 256), dtype=torch.uint8, device=device)
+    return buf, {name: buf[o:o + n].view(dtype).view(*shape) for name, dtype, shape, o, n in spans}
+
+
 class DeviceStep:
-    """All device buffers of one DSA layer-step for a generated workload."""
+    """All device buffers of one DSA layer-step for a generated workload.
+
+    The per-step inputs that change from step to step (row maps, page table,
+    q_idx, w, q) live in one device arena, `inputs`, and the outputs (out,
+    lse) in another, `outputs`, so a serving loop moves them with one copy
+    each way; t[...] are views into them."""
 
     def __init__(self, inp: dict, device="cuda", **cfg_override):
         wl = inp["workload"]
@@ -32,27 +52,32 @@ class DeviceStep:
         dsa.dsa_validate_config(self.cfg)
         self.rows = dsa.dsa_build_rows(self.cfg, inp["cache_len"], inp["new_tokens"])
         R, Hq, D = wl.max_rows, wl.num_q_heads, wl.head_dim
-        t = {}
-        t["page_table"] = to_device(inp["page_table"], device)
-        for k in ("row_req", "row_len", "block_first", "block_nrows"):
-            t[k] = to_device(self.rows[k], device)
-        t["q_idx"] = to_device(inp["q_idx"], device, "bf16")
-        t["w"] = to_device(inp["w"], device)
+        pt = np.ascontiguousarray(inp["page_table"])
+        self.inputs, t = _arena(
+            [(k, torch.int32, (R,)) for k in DEVICE_ROW_KEYS]
+            + [("page_table", torch.int32, pt.shape),
+               ("q_idx", torch.bfloat16, inp["q_idx"].shape),
+               ("w", torch.float32, inp["w"].shape),
+               ("q", torch.bfloat16, inp["q"].shape)], device)
+        for k in DEVICE_ROW_KEYS:
+            t[k].copy_(torch.from_numpy(self.rows[k]))
+        t["page_table"].copy_(torch.from_numpy(pt))
+        for k, kind in (("q_idx", "bf16"), ("w", "raw"), ("q", "bf16")):
+            t[k].copy_(to_device(inp[k], device, kind))
         if inp["idx_scale"] is None:
             t["idx_cache"] = to_device(inp["idx_cache"], device, "bf16")
             t["idx_scale"] = None
         else:
             t["idx_cache"] = to_device(inp["idx_cache"], device)
             t["idx_scale"] = to_device(inp["idx_scale"], device)
-        t["q"] = to_device(inp["q"], device, "bf16")
         t["k_cache"] = to_device(inp["k_cache"], device, "bf16")
         t["v_cache"] = to_device(inp["v_cache"], device, "bf16")
         if self.cfg.flags & dsa.DSA_FLAG_KV_INTERLEAVED:
             # one cache [NP, P, 2, Hkv, D]: each token's K row, then its V row
             kv = torch.stack((t["k_cache"], t["v_cache"]), dim=2).contiguous()
             t["k_cache"], t["v_cache"] = kv, kv[:, :, 1]
-        t["out"] = torch.zeros(R, Hq, D, dtype=torch.bfloat16, device=device)
-        t["lse"] = torch.zeros(R, Hq, dtype=torch.float32, device=device)
+        self.outputs, outs = _arena([("out", torch.bfloat16, (R, Hq, D)), ("lse", torch.float32, (R, Hq))], device)
+        t.update(outs)
         self.t = t
         self.workspace = dsa.alloc_workspace(self.cfg, device)
         self.views = dsa.workspace_views(self.cfg, self.workspace)
