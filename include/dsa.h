@@ -194,6 +194,23 @@ dsa_status_t dsa_workspace_layout(const dsa_config_t *cfg, dsa_workspace_layout_
  */
 dsa_status_t dsa_score_windows(const dsa_config_t *cfg, int32_t *window_rows, int32_t *num_windows);
 
+/*
+ * dsa_suggest_num_splits -- a num_splits for this config's row count and
+ * top-k on a GPU with num_sms SMs (num_sms <= 0: the current device's).
+ * Host only; no launch.  A tuning aid measured on GB300, not part of the
+ * method: the sparse attention runs one program per (row, split) on two
+ * resident CTAs per SM (C = 2 * num_sms).  It suggests
+ *   cap = min(64, max(1, topk / 32))        (>= 32 selected keys per split)
+ *   S4  = round(4 * C / max_rows)           (about four programs per CTA)
+ *   S1  = max(1, floor(C / max_rows))       (one wave of programs)
+ *   S   = S4 <= cap ? max(1, S4) : min(cap, S1)
+ * e.g. on 152 SMs: 64 rows, top-k 2048 -> 19; 8 rows, top-k 512 -> 16;
+ * 16 rows -> 19; 1024 rows -> 1.
+ * Errors: DSA_ERR_INVALID_ARG (bad config, NULL), DSA_ERR_CUDA (num_sms <= 0
+ * and no device to query).
+ */
+dsa_status_t dsa_suggest_num_splits(const dsa_config_t *cfg, int32_t num_sms, int32_t *num_splits);
+
 /* Clears the device status word (an async 4-byte memset on `stream`).
  * Call once after allocating a workspace and after reading a failure. */
 dsa_status_t dsa_reset_device_status(void *workspace, dsa_stream_t stream);

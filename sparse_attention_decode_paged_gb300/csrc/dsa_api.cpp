@@ -179,6 +179,24 @@ dsa_status_t dsa_workspace_size(const dsa_config_t *cfg, size_t *bytes) {
   return ok();
 }
 
+dsa_status_t dsa_suggest_num_splits(const dsa_config_t *cfg, int32_t num_sms, int32_t *num_splits) {
+  DSA_CHECK_CFG(cfg);
+  if (num_splits == nullptr) return fail(DSA_ERR_INVALID_ARG, "num_splits is NULL");
+  if (num_sms <= 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e, "SM count");
+    num_sms = sms;
+  }
+  const long long C = 2LL * num_sms, R = cfg->max_rows;
+  const long long cap = std::min<long long>(64, std::max(1, cfg->topk / 32));
+  const long long s4 = (4 * C + R / 2) / R;
+  const long long s1 = std::max<long long>(1, C / R);
+  *num_splits = static_cast<int32_t>(s4 <= cap ? std::max<long long>(1, s4) : std::min(cap, s1));
+  return ok();
+}
+
 dsa_status_t dsa_reset_device_status(void *workspace, dsa_stream_t stream) {
   DSA_CHECK_DEV_PTR(workspace);
   return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), stream), "reset status");

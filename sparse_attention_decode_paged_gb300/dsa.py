@@ -41,6 +41,7 @@ DSA_FLAG_KV_INTERLEAVED = 1 << 1
 EXPORTED = (
     "dsa_validate_config", "dsa_workspace_size", "dsa_workspace_layout",
     "dsa_reset_device_status", "dsa_read_device_status", "dsa_build_rows", "dsa_score_windows",
+    "dsa_suggest_num_splits",
     "dsa_indexer_scores", "dsa_indexer_scores_window", "dsa_topk", "dsa_topk_window",
     "dsa_sparse_attn", "dsa_merge", "dsa_step",
     "dsa_step_noalloc", "dsa_last_error", "dsa_version",
@@ -90,6 +91,7 @@ def _load():
         "dsa_read_device_status": [vp, ctypes.POINTER(ctypes.c_uint32), vp],
         "dsa_build_rows": [cfgp, i32] + [vp] * 7 + [i32p, i32p],
         "dsa_score_windows": [cfgp, i32p, i32p],
+        "dsa_suggest_num_splits": [cfgp, i32, i32p],
         "dsa_indexer_scores": [cfgp] + [vp] * 12,
         "dsa_indexer_scores_window": [cfgp, i32, i32] + [vp] * 12,
         "dsa_topk": [cfgp] + [vp] * 5,
@@ -279,6 +281,14 @@ def dsa_build_rows(cfg: dsa_config_t, req_cache_len, req_new_tokens, out=None) -
     outs["num_rows"] = int(nr.value)
     outs["num_blocks"] = int(nb.value)
     return outs
+
+
+def dsa_suggest_num_splits(cfg, num_sms: int = 0) -> int:
+    """A num_splits for cfg's rows and top-k on num_sms SMs (0: the current
+    device's); a tuning aid, see include/dsa.h."""
+    s = ctypes.c_int32()
+    _check(_lib.dsa_suggest_num_splits(ctypes.byref(cfg), int(num_sms), ctypes.byref(s)))
+    return int(s.value)
 
 
 def dsa_score_windows(cfg) -> tuple:

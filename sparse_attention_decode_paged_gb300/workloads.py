@@ -76,13 +76,15 @@ def _wl(name, seed, **kw) -> Workload:
     return Workload(name=name, seed=seed, **kw)
 
 
+# num_splits: what dsa_suggest_num_splits gives on a 152-SM GB300 (the
+# tiny case keeps 2 so the merge of split partials runs on it too)
 WORKLOADS = [
     _wl("tiny_decode_b2", 0, num_q_heads=4, num_kv_heads=1, head_dim=64,
         idx_heads=4, idx_dim=32, page_size=16, topk=16, num_splits=2,
         max_rows=2, max_reqs=2, max_pages_per_req=16, score_width=256,
         block_rows=1, idx_key_dtype=KEY_BF16, kind="decode"),
     _wl("decode_b8_l512_4096", 1, num_q_heads=64, num_kv_heads=8, head_dim=128,
-        idx_heads=64, idx_dim=128, page_size=64, topk=512, num_splits=4,
+        idx_heads=64, idx_dim=128, page_size=64, topk=512, num_splits=16,
         max_rows=8, max_reqs=8, max_pages_per_req=64, score_width=4096,
         block_rows=1, idx_key_dtype=KEY_BF16, kind="decode"),
     _wl("decode_b64_l32768_topk2048", 2, num_q_heads=64, num_kv_heads=8,
@@ -91,11 +93,11 @@ WORKLOADS = [
         score_width=32768, block_rows=1, idx_key_dtype=KEY_BF16, kind="decode"),
     _wl("mixed_48dec_512prefill", 3, num_q_heads=64, num_kv_heads=8,
         head_dim=128, idx_heads=64, idx_dim=128, page_size=64, topk=2048,
-        num_splits=4, max_rows=1024, max_reqs=49, max_pages_per_req=512,
+        num_splits=1, max_rows=1024, max_reqs=49, max_pages_per_req=512,
         score_width=32768, block_rows=4, idx_key_dtype=KEY_BF16, kind="mixed"),
     _wl("long_fp8_b16_l1024_131072", 4, num_q_heads=64, num_kv_heads=8,
         head_dim=128, idx_heads=64, idx_dim=128, page_size=64, topk=2048,
-        num_splits=8, max_rows=16, max_reqs=16, max_pages_per_req=2048,
+        num_splits=19, max_rows=16, max_reqs=16, max_pages_per_req=2048,
         score_width=131072, block_rows=1, idx_key_dtype=KEY_FP8_E4M3,
         kind="decode"),
 ]

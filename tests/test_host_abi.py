@@ -186,3 +186,42 @@ def test_kv_interleaved_requires_adjacent_v(dsa_lib):
 def lib_last_error(lib):
     lib.dsa_last_error.restype = ctypes.c_char_p
     return lib.dsa_last_error().decode()
+
+
+# ----------------------------------------------------------------------------
+# dsa_suggest_num_splits: the documented rule, on the host
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("rows,topk,sms,want", [
+    (64, 2048, 152, 19),    # 4 programs per resident CTA: round(4 * 304 / 64)
+    (8, 512, 152, 16),      # capped at topk / 32, one wave instead
+    (16, 2048, 152, 19),    # round(4 * 304 / 16) = 76 > cap 64: one wave, 304 // 16
+    (1024, 2048, 152, 1),
+    (2, 16, 152, 1),        # topk / 32 = 0: at least one split
+    (64, 2048, 76, 10),     # half the SMs: round(4 * 152 / 64) = round(9.5)
+    (4096, 2048, 152, 1),
+    (1, 4096, 152, 64),     # cap at 64
+])
+def test_suggest_num_splits_rule(rows, topk, sms, want, dsa_lib):
+    cfg = _cfg(dsa_lib, max_rows=rows, max_reqs=rows, topk=topk)
+    assert dsa_lib.dsa_suggest_num_splits(cfg, sms) == want
+    # what it suggests is itself a valid config
+    dsa_lib.dsa_validate_config(_cfg(dsa_lib, max_rows=rows, max_reqs=rows, topk=topk, num_splits=want))
+
+
+def test_suggest_num_splits_matches_the_workloads(dsa_lib):
+    """The parity workloads use the suggestion for a 152-SM GB300 (the tiny
+    case keeps 2 splits so the merge runs on it)."""
+    for i in range(1, 5):
+        wl = W.workload(i)
+        assert dsa_lib.dsa_suggest_num_splits(dsa_lib.config_from_workload(wl, 1000), 152) == wl.num_splits
+
+
+def test_suggest_num_splits_needs_a_device_or_a_count(dsa_lib):
+    import torch
+    cfg = _cfg(dsa_lib)
+    if torch.cuda.is_available():
+        assert 1 <= dsa_lib.dsa_suggest_num_splits(cfg) <= 64
+    else:
+        with pytest.raises(dsa_lib.DsaError) as e:
+            dsa_lib.dsa_suggest_num_splits(cfg)
+        assert e.value.status == dsa_lib.DSA_ERR_CUDA
