@@ -62,7 +62,7 @@ typedef struct CUstream_st *dsa_stream_t;
 typedef enum {
   DSA_OK = 0,
   DSA_ERR_INVALID_ARG = 1,   /* bad pointer, size or config field          */
-  DSA_ERR_UNSUPPORTED = 2,   /* valid shape this build has no kernel for   */
+  DSA_ERR_UNSUPPORTED = 2,   /* valid shape this library has no kernel for */
   DSA_ERR_CAPACITY = 3,      /* inputs exceed the config's static capacity */
   DSA_ERR_CUDA = 4,          /* a CUDA runtime call failed                 */
   DSA_ERR_DEVICE_BOUNDS = 5  /* the device status word is non-zero         */
@@ -82,7 +82,7 @@ typedef enum { DSA_KEY_BF16 = 0, DSA_KEY_FP8_E4M3 = 1 } dsa_key_dtype_t;
 
 /*
  * Model shape and static capacity; fixed for the lifetime of a captured
- * graph.  Supported by this build:
+ * graph.  Supported by this library:
  *   num_q_heads % num_kv_heads == 0, num_q_heads / num_kv_heads <= 8,
  *   num_kv_heads <= 8, head_dim in {64, 128}, max_rows <= 4096;
  *   1 <= idx_heads <= 64, idx_dim in {32, 64, 128};
