@@ -70,7 +70,10 @@ def _topk_cfg(dsa_lib, R, W_, K):
                                max_pages_per_req=(W_ + 63) // 64, score_width=W_, num_pages=1)
 
 
-@pytest.mark.parametrize("W_,K", [(4096, 512), (32768, 2048), (131072, 2048), (300, 16)])
+# widths reach each cluster size: 1 CTA (300, 4096), 2 (32768), 4 (65536,
+# 131072) and 8 (262144, the longest row the top-k takes)
+@pytest.mark.parametrize("W_,K", [(4096, 512), (32768, 2048), (65536, 1024), (131072, 2048), (262144, 2048),
+                                  (300, 16)])
 def test_topk_crafted_rows(W_, K, dsa_lib, cuda_ok):
     rng = np.random.default_rng(W_ + K)
     R = 12
