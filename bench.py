@@ -286,7 +286,10 @@ def cpu_baseline_worker(path: str):
     print(json.dumps({"times": times}))
 
 
-def run_cpu_baseline(inp, wl_index: int, rows_total: int, reps: int = 6):
+def oracle_times(inp, wl_index: int, reps: int) -> list:
+    """Seconds per pass of the CPU oracle over a bounded sample of the
+    workload (CPU_SAMPLE_ROWS full rows), `reps` passes, in a child process
+    whose BLAS / OpenMP pools are held to one thread."""
     sub_wl, arrays = cpu_sample(inp, CPU_SAMPLE_ROWS)
     with tempfile.TemporaryDirectory() as td:
         path = os.path.join(td, "sample.npz")
@@ -298,8 +301,15 @@ def run_cpu_baseline(inp, wl_index: int, rows_total: int, reps: int = 6):
         r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker", path],
                            capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
-        return {"error": r.stderr.strip()[-300:]}
-    times = json.loads(r.stdout.strip().splitlines()[-1])["times"]
+        raise RuntimeError(r.stderr.strip()[-300:])
+    return json.loads(r.stdout.strip().splitlines()[-1])["times"]
+
+
+def run_cpu_baseline(inp, wl_index: int, rows_total: int, reps: int = 6):
+    try:
+        times = oracle_times(inp, wl_index, reps)
+    except RuntimeError as exc:
+        return {"error": str(exc)}
     per_step_s = statistics.median(times) * rows_total / CPU_SAMPLE_ROWS
     return {"value": per_step_s * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
             "sample": f"{CPU_SAMPLE_ROWS} of {rows_total} rows (full rows: indexer over all 32768 keys, "
@@ -319,16 +329,15 @@ def run_reference(args):
     wl = inp["workload"]
     from oracle import dsa_oracle as O
     rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
-    sub_wl, arrays = cpu_sample(inp, CPU_SAMPLE_ROWS)
-    del inp
-    time_oracle(sub_wl, arrays, max(args.warmup, 0))
     t0 = time.perf_counter()
-    times = time_oracle(sub_wl, arrays, args.steps)
+    # warm-up passes first, then the timed ones, in a one-thread child process
+    times = oracle_times(inp, args.workload, max(args.warmup, 0) + args.steps)[max(args.warmup, 0):]
     wall = time.perf_counter() - t0
     scale = rows["num_rows"] / CPU_SAMPLE_ROWS
     us = statistics.mean(times) * scale * 1e6
     sample = (f"{CPU_SAMPLE_ROWS} of {rows['num_rows']} rows per step (full rows), scaled by "
-              f"{rows['num_rows']}/{CPU_SAMPLE_ROWS}; fp64 numpy, one thread")
+              f"{rows['num_rows']}/{CPU_SAMPLE_ROWS}; fp64 numpy, one thread (BLAS and OpenMP pools held "
+              f"to one thread in a child process)")
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
