@@ -144,8 +144,6 @@ def test_attention_vs_oracle_on_gpu_selection(problem):
 
 def test_split_partials_vs_oracle(problem):
     i, inp, dev = problem
-    if i not in (0, 1, 3):
-        pytest.skip("partials checked on workloads 0, 1, 3")
     wl = inp["workload"]
     rows = _rows(inp)
     idx = dev.views["topk_idx"].cpu().numpy()
