@@ -225,3 +225,33 @@ def test_suggest_num_splits_needs_a_device_or_a_count(dsa_lib):
         with pytest.raises(dsa_lib.DsaError) as e:
             dsa_lib.dsa_suggest_num_splits(cfg)
         assert e.value.status == dsa_lib.DSA_ERR_CUDA
+
+
+# ----------------------------------------------------------------------------
+# the harness's input / output arenas (host logic, CPU tensors)
+# ----------------------------------------------------------------------------
+def test_arena_views_are_aligned_disjoint_and_shaped():
+    import torch
+    from sparse_attention_decode_paged_gb300.harness import DEVICE_ROW_KEYS, _arena
+
+    R = 3  # a row count whose int32 arrays are not a multiple of 16 bytes
+    parts = [(k, torch.int32, (R,)) for k in DEVICE_ROW_KEYS] + [
+        ("page_table", torch.int32, (3, 5)), ("q_idx", torch.bfloat16, (R, 4, 32)),
+        ("w", torch.float32, (R, 4)), ("q", torch.bfloat16, (R, 4, 64))]
+    buf, views = _arena(parts, "cpu")
+    spans = []
+    for name, dtype, shape in parts:
+        v = views[name]
+        assert v.dtype == dtype and tuple(v.shape) == shape and v.is_contiguous()
+        off = v.data_ptr() - buf.data_ptr()
+        assert off % 256 == 0, name  # every view meets the library's 16-byte pointer rule
+        spans.append((off, off + v.numel() * v.element_size()))
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))  # no overlap
+    assert spans[-1][1] <= buf.numel()
+    # writes through one view land in the buffer a single copy moves
+    views["q"].fill_(1.5)
+    views["row_len"].copy_(torch.tensor([7, 8, 9], dtype=torch.int32))
+    again = {n: buf[v.data_ptr() - buf.data_ptr():][:v.numel() * v.element_size()] for n, v in views.items()}
+    assert torch.equal(again["row_len"].view(torch.int32), torch.tensor([7, 8, 9], dtype=torch.int32))
+    assert bool((again["q"].view(torch.bfloat16) == 1.5).all())
