@@ -8,9 +8,10 @@
 //
 // Each fp32 score maps to a 32-bit key whose unsigned order is the ranking
 // (NaN -> 0, -0 -> +0).  A row is split across a cluster of C CTAs (1024
-// threads each, C = ceil(W / 16K) up to 4, or ceil(W / 32K) -- 8 for rows
-// past 128K keys -- when the rows outnumber what the GPU holds at once),
-// each holding its contiguous segment of the row as keys in shared memory.
+// threads each; a CTA holds at most 32K keys, so C >= ceil(W / 32K), up to
+// 8; above that floor C = ceil(W / 16K) capped at 4, or the floor alone
+// when the rows outnumber what the GPU holds at once), each holding its
+// contiguous segment of the row as keys in shared memory.
 // One launch covers one row window (commit message 3): all rows, or those
 // of a score window, whose scores start at the window's first row.  Thread t of a CTA owns the
 // 4-key groups t, t + 1024, t + 2048, ... of the segment, so every pass over
