@@ -121,6 +121,7 @@ def _check(status: int):
 
 
 def version() -> str:
+    """The library's version string."""
     return _lib.dsa_version().decode()
 
 
@@ -131,6 +132,8 @@ def make_config(*, num_q_heads, num_kv_heads, head_dim, idx_heads, idx_dim, page
                 num_splits, max_rows, max_reqs, max_pages_per_req, score_width, num_pages,
                 block_rows=1, idx_key_dtype=DSA_KEY_BF16, sm_scale=None, flags=0,
                 score_buffer_bytes=0) -> dsa_config_t:
+    """A dsa_config_t (fields as in include/dsa.h); sm_scale defaults to
+    1/sqrt(head_dim).  Not validated here: see dsa_validate_config."""
     if sm_scale is None:
         sm_scale = 1.0 / float(np.sqrt(head_dim))
     return dsa_config_t(num_q_heads, num_kv_heads, head_dim, idx_heads, idx_dim, page_size, topk,
@@ -140,6 +143,8 @@ def make_config(*, num_q_heads, num_kv_heads, head_dim, idx_heads, idx_dim, page
 
 
 def config_from_workload(wl, num_pages: int, **override) -> dsa_config_t:
+    """The config of a generated workload (workloads.Workload) over a pool
+    of num_pages pages; keyword arguments override single fields."""
     kw = dict(num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
               idx_heads=wl.idx_heads, idx_dim=wl.idx_dim, page_size=wl.page_size,
               topk=wl.topk, num_splits=wl.num_splits, max_rows=wl.max_rows,
@@ -151,16 +156,19 @@ def config_from_workload(wl, num_pages: int, **override) -> dsa_config_t:
 
 
 def dsa_validate_config(cfg: dsa_config_t) -> None:
+    """Raises DsaError if the library has no kernel for this config."""
     _check(_lib.dsa_validate_config(ctypes.byref(cfg)))
 
 
 def dsa_workspace_size(cfg: dsa_config_t) -> int:
+    """Bytes of device workspace dsa_step needs for this config."""
     n = ctypes.c_size_t(0)
     _check(_lib.dsa_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
     return int(n.value)
 
 
 def dsa_workspace_layout(cfg: dsa_config_t) -> dict:
+    """Byte offsets of the step's intermediates inside the workspace."""
     lay = dsa_workspace_layout_t()
     _check(_lib.dsa_workspace_layout(ctypes.byref(cfg), ctypes.byref(lay)))
     return {name: int(getattr(lay, name)) for name, _ in lay._fields_}
@@ -234,6 +242,7 @@ def workspace_views(cfg: dsa_config_t, workspace: torch.Tensor) -> dict:
 # entry points
 # ----------------------------------------------------------------------------
 def dsa_reset_device_status(workspace, stream=None) -> None:
+    """Clears the workspace's sticky device status word (async on stream)."""
     _check(_lib.dsa_reset_device_status(_ws(workspace), _stream(stream)))
 
 
@@ -353,6 +362,9 @@ def _kv_ptrs(cfg, k_cache, v_cache):
 
 def dsa_sparse_attn(cfg, q, k_cache, v_cache, page_table, row_req, row_len, topk_idx, part_m,
                     part_l, part_acc, workspace, stream=None) -> None:
+    """Split sparse GQA attention over topk_idx: partial m, l [R, Hq, S] and
+    acc [R, Hq, S, D] (fp32).  With DSA_FLAG_KV_INTERLEAVED, k_cache is the
+    one interleaved cache and v_cache may be None."""
     R, Hq, S, D = cfg.max_rows, cfg.num_q_heads, cfg.num_splits, cfg.head_dim
     k_ptr, v_ptr = _kv_ptrs(cfg, k_cache, v_cache)
     _check(_lib.dsa_sparse_attn(
@@ -367,6 +379,8 @@ def dsa_sparse_attn(cfg, q, k_cache, v_cache, page_table, row_req, row_len, topk
 
 
 def dsa_merge(cfg, part_m, part_l, part_acc, out, lse=None, stream=None) -> None:
+    """Merges the split partials into out (bf16 [R, Hq, D]) and, if given,
+    lse (fp32 [R, Hq])."""
     R, Hq, S, D = cfg.max_rows, cfg.num_q_heads, cfg.num_splits, cfg.head_dim
     _check(_lib.dsa_merge(
         ctypes.byref(cfg), _dev(part_m, "part_m", (torch.float32,), R * Hq * S),
