@@ -390,7 +390,9 @@ dsa_status_t dsa_step_noalloc(const dsa_config_t *cfg, const dsa_step_args_t *ar
 /* Text of the last error on the calling thread ("" if none). */
 const char *dsa_last_error(void);
 
-/* Library version string. */
+/* Library version string.  0.2: dsa_config_t gained score_buffer_bytes
+ * (its size changed; rebuild callers), and the _window calls,
+ * dsa_score_windows and dsa_suggest_num_splits were added. */
 const char *dsa_version(void);
 
 #ifdef __cplusplus

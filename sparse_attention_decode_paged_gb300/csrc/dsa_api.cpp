@@ -496,6 +496,6 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *a, void *w
 
 const char *dsa_last_error(void) { return g_last_error.c_str(); }
 
-const char *dsa_version(void) { return "dsa-gb300 0.1 (sm_103a)"; }
+const char *dsa_version(void) { return "dsa-gb300 0.2 (sm_103a)"; }
 
 }  // extern "C"

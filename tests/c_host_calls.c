@@ -6,6 +6,7 @@
  * Prints "ok" and exits 0 when every check holds; tests/test_c_host.py
  * compiles and runs it.
  */
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -47,8 +48,21 @@ static dsa_config_t decode_config(void) {
   return c;
 }
 
-int main(void) {
+int main(int argc, char **argv) {
   dsa_config_t cfg = decode_config();
+  /* the struct layouts the Python binding mirrors (argv[1..4]: its sizes
+   * and the offset of score_buffer_bytes) */
+  if (argc == 5) {
+    long want[4];
+    int i;
+    for (i = 0; i < 4; ++i) sscanf(argv[i + 1], "%ld", &want[i]);
+    CHECK((long)sizeof(dsa_config_t) == want[0]);
+    CHECK((long)offsetof(dsa_config_t, score_buffer_bytes) == want[1]);
+    CHECK((long)sizeof(dsa_step_args_t) == want[2]);
+    CHECK((long)sizeof(dsa_workspace_layout_t) == want[3]);
+  } else {
+    CHECK(argc == 1);
+  }
   CHECK(strlen(dsa_version()) > 0);
   CHECK(dsa_validate_config(&cfg) == DSA_OK);
 
