@@ -286,14 +286,14 @@ def cpu_baseline_worker(path: str):
     print(json.dumps({"times": times}))
 
 
-def oracle_times(inp, wl_index: int, reps: int) -> list:
+def oracle_times(inp, wl_index: int, reps: int, nrows: int = CPU_SAMPLE_ROWS) -> list:
     """Seconds per pass of the CPU oracle over a bounded sample of the
-    workload (CPU_SAMPLE_ROWS full rows), `reps` passes, in a child process
-    whose BLAS / OpenMP pools are held to one thread."""
-    sub_wl, arrays = cpu_sample(inp, CPU_SAMPLE_ROWS)
+    workload (nrows full rows), `reps` passes, in a child process whose BLAS
+    / OpenMP pools are held to one thread."""
+    sub_wl, arrays = cpu_sample(inp, nrows)
     with tempfile.TemporaryDirectory() as td:
         path = os.path.join(td, "sample.npz")
-        meta = json.dumps({"workload": wl_index, "nrows": CPU_SAMPLE_ROWS, "reps": reps})
+        meta = json.dumps({"workload": wl_index, "nrows": nrows, "reps": reps})
         np.savez(path, meta=np.array(meta), **arrays)
         env = dict(os.environ)
         for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
@@ -329,14 +329,19 @@ def run_reference(args):
     wl = inp["workload"]
     from oracle import dsa_oracle as O
     rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+    # a step samples fewer rows when many steps are asked for, so the whole
+    # run stays within a few minutes (a pass over one 32K-key row takes
+    # ~0.08 s on one core)
+    passes = max(args.warmup, 0) + args.steps
+    nrows = CPU_SAMPLE_ROWS if passes <= 600 else 1
     t0 = time.perf_counter()
     # warm-up passes first, then the timed ones, in a one-thread child process
-    times = oracle_times(inp, args.workload, max(args.warmup, 0) + args.steps)[max(args.warmup, 0):]
+    times = oracle_times(inp, args.workload, passes, nrows)[max(args.warmup, 0):]
     wall = time.perf_counter() - t0
-    scale = rows["num_rows"] / CPU_SAMPLE_ROWS
+    scale = rows["num_rows"] / nrows
     us = statistics.mean(times) * scale * 1e6
-    sample = (f"{CPU_SAMPLE_ROWS} of {rows['num_rows']} rows per step (full rows), scaled by "
-              f"{rows['num_rows']}/{CPU_SAMPLE_ROWS}; fp64 numpy, one thread (BLAS and OpenMP pools held "
+    sample = (f"{nrows} of {rows['num_rows']} rows per step (full rows), scaled by "
+              f"{rows['num_rows']}/{nrows}; fp64 numpy, one thread (BLAS and OpenMP pools held "
               f"to one thread in a child process)")
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": args.gpus,
