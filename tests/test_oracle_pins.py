@@ -270,6 +270,41 @@ def test_attention_worked_example(golden_dir):
     np.testing.assert_allclose(lse, g["lse"], rtol=1e-15, atol=1e-15)
 
 
+def _paged_golden_input(g):
+    wl = _tiny_wl(page_size=g["page_size"], num_q_heads=g["num_q_heads"], num_kv_heads=g["num_kv_heads"],
+                  head_dim=g["head_dim"], max_rows=len(g["cache_len"]), max_reqs=len(g["cache_len"]),
+                  max_pages_per_req=len(g["page_table"][0]), topk=len(g["topk_idx"][0]), block_rows=1)
+    assert wl.sm_scale == 0.5  # the fixture's scale, 1/sqrt(4)
+    inp = dict(workload=wl, cache_len=np.array(g["cache_len"]), new_tokens=np.array(g["new_tokens"]),
+               page_table=np.array(g["page_table"], np.int32), q=_bf16_bits(g["q"]),
+               k_cache=_bf16_bits(g["k_cache"]), v_cache=_bf16_bits(g["v_cache"]))
+    rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+    return inp, rows
+
+
+def test_paged_kv_rows_worked_example(golden_dir):
+    # the paged fetch alone: K and V of the selected logical positions, through
+    # the page table, each from its own cache
+    g = _golden(golden_dir, "paged_attention_worked_example.json")
+    inp, rows = _paged_golden_input(g)
+    for r in range(2):
+        k, v = O.kv_rows(inp, int(rows["row_req"][r]), g["topk_idx"][r])
+        assert np.array_equal(k, np.array(g["selected_k"][r], np.float64)), r
+        assert np.array_equal(v, np.array(g["selected_v"][r], np.float64)), r
+
+
+def test_paged_attention_worked_example(golden_dir):
+    # the whole paged driver (rows -> request -> page table -> K, V ->
+    # softmax) against the hand-worked closed form: a K/V swap, a page/slot
+    # mix-up or a wrong request's table changes every output
+    g = _golden(golden_dir, "paged_attention_worked_example.json")
+    inp, rows = _paged_golden_input(g)
+    assert rows["row_len"].tolist() == [4, 2]
+    out, lse = O.attention(inp, rows, np.array(g["topk_idx"], np.int32))
+    np.testing.assert_allclose(out, g["out"], rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(lse, g["lse"], rtol=1e-14, atol=1e-14)
+
+
 @pytest.mark.parametrize("hq,hkv", [(4, 1), (8, 2), (8, 4)])
 def test_attention_full_prefix_matches_sdpa(hq, hkv):
     # with top-k >= length the selection is the whole causal prefix and the
