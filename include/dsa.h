@@ -377,8 +377,11 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *args, void
  * device address (cudaGetSymbolAddress) with that device current, so make
  * that first call outside stream capture.  All calls on a device share the
  * array and it keeps the last call's contents; the status word is cleared at
- * the start of every call.  Calls whose executions overlap on the GPU (other
- * streams, concurrent graph replays) race on the array.
+ * the start of every call, and a call whose config lays the array out
+ * differently from the previous call's on that device first clears its key
+ * histogram region (an async memset on `stream`).  Calls whose executions
+ * overlap on the GPU (other streams, concurrent graph replays) race on the
+ * array.
  *
  * args: as dsa_step.  status_out: device uint32 (nullable, 4-byte aligned);
  * when given, the step's device status word is copied there at the end of

@@ -14,10 +14,15 @@
 // device address is looked up once per device with cudaGetSymbolAddress on
 // the first call made on that device (with the device current); that first
 // call must therefore happen outside stream capture.  All calls on a device
-// share the one array and it keeps the last call's contents: the status word
-// is cleared at the start of each call, everything else is fully rewritten
-// before it is read.  Calls whose executions overlap on the GPU (different
-// streams, or graphs replayed concurrently) race on the array.
+// share the one array and it keeps the last call's contents.  The status word
+// is cleared at the start of each call.  The key histogram must start at
+// zero: a step leaves its own histogram region at zero (the top-k clears
+// each row's counts after using them), but the region's offset and size
+// follow the config, so a call whose layout differs from the previous
+// call's on that device first clears its histogram region on `stream`.
+// Scores, top-k and partials are fully rewritten before they are read.
+// Calls whose executions overlap on the GPU (different streams, or graphs
+// replayed concurrently) race on the array.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -33,6 +38,10 @@ __device__ __align__(256) unsigned char g_step_scratch[kNoAllocScratchBytes];
 
 std::mutex g_scratch_mu;
 void *g_scratch_ptr[kMaxDevices] = {};
+// key-histogram region (offset, bytes) of the last call on each device; a
+// region of 0 bytes means unknown (no call yet, or a call that failed)
+size_t g_hist_off[kMaxDevices] = {};
+size_t g_hist_bytes[kMaxDevices] = {};
 
 }  // namespace
 
@@ -55,25 +64,34 @@ extern "C" dsa_status_t dsa_step_noalloc(const dsa_config_t *cfg, const dsa_step
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return dsa::set_error(DSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return dsa::set_error(DSA_ERR_UNSUPPORTED, "device %d", dev);
-  void *ws = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-      void *p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_step_scratch);
-      if (e != cudaSuccess)
-        return dsa::set_error(DSA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-      g_scratch_ptr[dev] = p;
-    }
-    ws = g_scratch_ptr[dev];
+  dsa_workspace_layout_t lay;
+  st = dsa_workspace_layout(cfg, &lay);
+  if (st != DSA_OK) return st;
+  const size_t hist_bytes = lay.total - lay.key_hist;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_step_scratch);
+    if (e != cudaSuccess)
+      return dsa::set_error(DSA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_scratch_ptr[dev] = p;
   }
+  char *ws = static_cast<char *>(g_scratch_ptr[dev]);
+  const bool same_layout = g_hist_bytes[dev] == hist_bytes && g_hist_off[dev] == lay.key_hist;
+  g_hist_bytes[dev] = 0;  // unknown until this call has been queued in full
   e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream);  // the status word starts at zero
   if (e != cudaSuccess) return dsa::set_error(DSA_ERR_CUDA, "clear status: %s", cudaGetErrorString(e));
+  if (!same_layout) {  // the new histogram region holds the previous call's other data
+    e = cudaMemsetAsync(ws + lay.key_hist, 0, hist_bytes, stream);
+    if (e != cudaSuccess) return dsa::set_error(DSA_ERR_CUDA, "clear histogram: %s", cudaGetErrorString(e));
+  }
   st = dsa_step(cfg, args, ws, stream);
   if (st != DSA_OK) return st;
   if (status_out != nullptr) {
     e = cudaMemcpyAsync(status_out, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream);
     if (e != cudaSuccess) return dsa::set_error(DSA_ERR_CUDA, "copy status: %s", cudaGetErrorString(e));
   }
+  g_hist_off[dev] = lay.key_hist;
+  g_hist_bytes[dev] = hist_bytes;
   return DSA_OK;
 }

@@ -165,3 +165,88 @@ def test_window_calls_match_whole(i, windows, dsa_lib, cuda_ok):
         covered[lo:hi] = True
     assert covered.all()
     assert torch.equal(sel, full_sel)
+
+
+# ----------------------------------------------------------------------------
+# GPU: a windowed step against the oracle
+# ----------------------------------------------------------------------------
+# sampled rows: on the mixed workload both sides of the window edge at row
+# 250, which cuts the prefill score block of rows 248..251, the edge at 500
+# (a block boundary), decode rows and pad rows; on the long fp8 workload
+# (5-row windows) every row
+_ORACLE_ROWS = {3: [0, 23, 47, 48, 49, 246, 247, 248, 249, 250, 251, 252, 253, 498, 499, 500, 501, 558, 559, 560,
+                    1023],
+                4: list(range(16))}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("i", [3, 4])
+def test_windowed_step_vs_oracle(i, dsa_lib, cuda_ok):
+    """A step with a score budget (several row windows) compared with the
+    oracle: each window's scores within the score tolerance, its top-k
+    bit-exact given those scores, and the windowed dsa_step's output and lse
+    on its own selection within the attention tolerance.  The selection is
+    also checked as a valid top-k under the oracle's own scores: every
+    selected position ranks within the score tolerance of the k-th best."""
+    from oracle import dsa_oracle as O
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    inp = W.generate(i)
+    wl = inp["workload"]
+    rtol = 6e-2 if wl.idx_key_dtype == W.KEY_FP8_E4M3 else 2e-2
+    dev = DeviceStep(inp, score_buffer_bytes=_WINDOW_ROWS[i] * wl.score_width * 4,
+                     flags=dsa_lib.DSA_FLAG_KV_INTERLEAVED)
+    cfg, t, v = dev.cfg, dev.t, dev.views
+    wr, nw = dsa_lib.dsa_score_windows(cfg)
+    assert nw > 1
+    dev.step()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    sel_step = v["topk_idx"].cpu().numpy()
+    out = dev.t["out"].float().cpu().numpy().astype(np.float64)
+    lse = dev.t["lse"].cpu().numpy().astype(np.float64)
+
+    rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+    qi = O.bf16_bits_to_f64(inp["q_idx"])
+    q = O.bf16_bits_to_f64(inp["q"])
+    sample = [r for r in _ORACLE_ROWS[i] if r < wl.max_rows]
+    # the window calls dsa_step makes, with each window's scores kept
+    idx_args = (t["q_idx"], t["w"], t["idx_cache"], t["idx_scale"], t["page_table"], t["row_req"],
+                t["row_len"], t["block_first"], t["block_nrows"])
+    sel = torch.full_like(v["topk_idx"], -7)
+    win_scores = {}
+    for lo in range(0, cfg.max_rows, wr):
+        hi = min(lo + wr, cfg.max_rows)
+        if not any(lo <= r < hi for r in sample):
+            continue
+        dsa_lib.dsa_indexer_scores(cfg, *idx_args, v["scores"], dev.workspace, window=(lo, hi))
+        dsa_lib.dsa_topk(cfg, v["scores"], t["row_len"], sel, dev.workspace, window=(lo, hi))
+        torch.cuda.synchronize()
+        got = v["scores"].cpu().numpy()
+        for r in range(lo, hi):
+            if r in sample:
+                win_scores[r] = got[r - lo].copy()
+    assert dev.status() == 0
+    sel = sel.cpu().numpy()
+    for r in sample:
+        L = int(rows["row_len"][r])
+        if L == 0:
+            assert (sel_step[r] == -1).all() and (out[r] == 0).all() and np.isneginf(lse[r]).all()
+            continue
+        keys, sc = O.index_keys(inp, int(rows["row_req"][r]), L)
+        want = O.indexer_scores_row(qi[r], inp["w"][r], keys, sc)
+        g = win_scores[r][:L].astype(np.float64)
+        rms = np.sqrt(np.mean(want * want))
+        assert np.all(np.abs(g - want) <= rtol * np.abs(want) + rtol * rms), f"scores, row {r}"
+        assert np.array_equal(sel[r], O.topk_row(win_scores[r], L, wl.topk)), f"top-k, row {r}"
+        assert np.array_equal(sel_step[r], sel[r]), f"step selection, row {r}"
+        chosen = sel_step[r][sel_step[r] >= 0]
+        n = min(wl.topk, L)
+        assert chosen.size == n and np.all(np.diff(chosen) > 0) and chosen[-1] < L
+        if n < L:  # valid under the oracle's scores up to the score tolerance
+            kth = np.sort(want)[::-1][n - 1]
+            assert np.all(want[chosen] >= kth - 2 * (rtol * np.abs(kth) + rtol * rms)), f"selection, row {r}"
+        k, vv = O.kv_rows(inp, int(rows["row_req"][r]), chosen)
+        o, ls = O.attention_row(q[r], k, vv, wl.sm_scale, wl.num_kv_heads)
+        np.testing.assert_allclose(out[r], o, atol=1e-2, rtol=2e-2, err_msg=f"row {r}")
+        np.testing.assert_allclose(lse[r], ls, atol=1e-2, rtol=2e-2, err_msg=f"row {r}")
