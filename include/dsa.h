@@ -87,7 +87,7 @@ typedef enum { DSA_KEY_BF16 = 0, DSA_KEY_FP8_E4M3 = 1 } dsa_key_dtype_t;
  *   num_kv_heads <= 8, head_dim in {64, 128}, max_rows <= 4096;
  *   1 <= idx_heads <= 64, idx_dim in {32, 64, 128};
  *   page_size in {16, 32, 64, 128}; 1 <= block_rows <= 4;
- *   1 <= topk <= score_width <= min(262144, max_pages_per_req * page_size);
+ *   1 <= topk <= score_width <= min(4194304, max_pages_per_req * page_size);
  *   1 <= num_splits <= 64; sm_scale > 0 and finite;
  *   score_buffer_bytes == 0 or >= score_width * 4 (one score row).
  */
@@ -295,6 +295,11 @@ dsa_status_t dsa_indexer_scores_window(const dsa_config_t *cfg, int32_t row_begi
  * [max_rows, topk].  Bit-exact and deterministic.  With
  * DSA_FLAG_TOPK_HISTOGRAM it starts from the workspace histogram the
  * indexer counted (checked against the row, see the flag) and zeroes it.
+ * Rows of up to 262144 keys are selected inside one thread-block cluster's
+ * shared memory; with a longer score_width every pass streams the row from
+ * `scores` instead, keeping on chip only the keys of the k-th key's
+ * first-level bin (commit message 4: past 64K keys, selection works on the
+ * candidates of a threshold); the result is the same.
  */
 dsa_status_t dsa_topk(const dsa_config_t *cfg, const float *scores, const int32_t *row_len,
                       int32_t *topk_idx, void *workspace, dsa_stream_t stream);

@@ -15,6 +15,11 @@
 
 namespace {
 
+// Longest row (keys) a config may ask for.  Rows up to 8 x 32K keys are
+// selected in one cluster's shared memory; longer ones by the streaming
+// top-k, whose passes read the score buffer.
+constexpr int32_t kMaxScoreWidth = 1 << 22;
+
 thread_local std::string g_last_error;
 
 dsa_status_t fail(dsa_status_t st, const char *fmt, ...) {
@@ -132,8 +137,8 @@ dsa_status_t dsa_validate_config(const dsa_config_t *c) {
                                 static_cast<long long>(c->max_pages_per_req) * c->page_size)
     return fail(DSA_ERR_INVALID_ARG, "score_width %d must be in [1, max_pages_per_req * page_size]",
                 c->score_width);
-  if (c->score_width > 262144)
-    return fail(DSA_ERR_UNSUPPORTED, "score_width %d > 262144 (8 top-k CTAs x 32K keys)", c->score_width);
+  if (c->score_width > kMaxScoreWidth)
+    return fail(DSA_ERR_UNSUPPORTED, "score_width %d > %d", c->score_width, kMaxScoreWidth);
   if (c->topk < 1 || c->topk > c->score_width)
     return fail(DSA_ERR_INVALID_ARG, "topk %d must be in [1, score_width]", c->topk);
   if (c->num_splits < 1 || c->num_splits > 64)

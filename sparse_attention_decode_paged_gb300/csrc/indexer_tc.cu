@@ -53,6 +53,7 @@ constexpr int kWarps = 10;  // 0 producer, 1 MMA, 2..5 and 6..9 two epilogue war
 constexpr int kThreads = kWarps * 32;
 constexpr long long kWaitBudget = 2000000000LL;  // SM cycles (about 1 s)
 constexpr int kMaxRowsTc = 4096;                  // prefix table capacity
+constexpr int kMaxStages = 16;                    // key-tile ring depth at most
 
 struct TcLayout {
   int hp;         // indexer heads padded to a multiple of 16
@@ -725,7 +726,8 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
   int cols = 32;
   while (cols < lay.nacc * lay.n_max) cols <<= 1;
   lay.tmem_cols = cols;
-  // One CTA per SM: the deep key ring (up to 6 stages of 32 KiB) hides the
+  // One CTA per SM: the deep key ring (as many stages as shared memory
+  // holds: 6 of 32 KiB for bf16 keys, 12 of 16 KiB for fp8 keys) hides the
   // MMA/epilogue round trip; the floor keeps a second CTA (and a second TMEM
   // owner) off the SM.
   const int ctas_per_sm = 1;
@@ -738,7 +740,7 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
     off += nq * lay.n_max * 4;                    // weights
     off += (cfg.max_rows + 1) * 4 + 16;           // prefix table
     off += kBlkCache * 8 * 4;                     // block cache
-    off += (2 * 8 + 13) * 8 + 64;                 // barriers (upper bound) + misc
+    off += (2 * kMaxStages + 13) * 8 + 64;        // barriers (upper bound) + misc
     return off + 1024 + 34 * 4;                   // alignment slack, scan scratch
   };
   lay.nq = 2;
@@ -747,7 +749,7 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
     lay.nq = 1;
     stages = static_cast<int>((kSmemLimit - fixed(1)) / stageB);
   }
-  stages = stages > 8 ? 8 : stages;
+  stages = stages > kMaxStages ? kMaxStages : stages;
   if (stages < 2) return cudaErrorInvalidValue;
   lay.stages = stages;
   uint32_t off = stages * stageB;

@@ -70,7 +70,8 @@ struct TopkShared {
 // Finds, scanning bins from the top, the bin d with above(d) < need <=
 // above(d) + hist[d]; writes d and above(d) to sh.digit / sh.above, or nbins
 // and 0 when the histogram holds fewer than `need` keys.
-__device__ __forceinline__ void select_bin(TopkShared &sh, const uint32_t *hist, int nbins, uint32_t need) {
+template <class SH>
+__device__ __forceinline__ void select_bin(SH &sh, const uint32_t *hist, int nbins, uint32_t need) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = nbins / kThreads;  // 1 or 4 bins per thread, descending
   uint32_t c[4] = {0u, 0u, 0u, 0u}, tot = 0u;
@@ -138,7 +139,8 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane) {
 // One radix pass over `cnt` keys: histogram of bits [shift, shift+10) of the
 // keys matching prefix/mask, then the bin of the need-th key.  Returns the
 // bin (clamped; sh.digit == kBins2 flags a histogram that came up short).
-__device__ __forceinline__ uint32_t radix_pass(TopkShared &sh, const uint32_t *keys, uint32_t cnt, int shift,
+template <class SH>
+__device__ __forceinline__ uint32_t radix_pass(SH &sh, const uint32_t *keys, uint32_t cnt, int shift,
                                                uint32_t prefix, uint32_t mask, uint32_t &need) {
   const int tid = threadIdx.x;
   for (int i = tid; i < kBins2; i += kThreads) sh.hist_tot[i] = 0u;
@@ -454,6 +456,316 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
   cl.sync();  // keep this CTA's shared memory alive until the cluster is done with it
 }
 
+// ---------------------------------------------------------------------------
+// Rows longer than a cluster's shared memory holds (score_width > 8 x 32K):
+// the same selection, with every pass streaming the row's scores from the
+// score buffer instead of shared memory (commit message 4: past 64K keys the
+// selection should touch only the candidates of the threshold; here the
+// indexer's exact first-level histogram names the k-th key's bin before any
+// score is read, so a pass keeps only that bin's keys on chip).
+//
+// One cluster of kStreamCluster CTAs per row; CTA q owns a contiguous
+// segment of the row and warp w of the CTA a contiguous range of that
+// segment, read in steps of kStreamU float4 loads per lane:
+//  A. the row's histogram: the indexer's counts if they total the row
+//     length, else counted in one pass and summed over the cluster;
+//  B. the bin of the k-th key; C. one pass copies out the keys inside it
+//     (at most kCandMax for the row, then two radix passes over them in
+//     shared memory) or, for heavier bins, two passes refine the threshold
+//     10 bits at a time;
+//  D. one pass counts, per warp, the keys above the threshold key tau and
+//     equal to it; warp and cluster prefixes of those counts then give, in a
+//     second pass, every selected key its rank in ascending position order.
+// Integer work on the same keys as the in-shared-memory kernel, so the
+// result is the same, bit for bit.
+// ---------------------------------------------------------------------------
+constexpr int kStreamCluster = 8;
+constexpr int kStreamU = 4;                               // float4 loads per lane and step
+constexpr int kStreamStep = 4 * 32 * kStreamU;            // keys per warp step
+constexpr int kStreamSegAlign = kStreamStep * kWarps;     // a CTA segment is a multiple of this
+
+struct StreamShared {
+  uint32_t hist[kBins1];        // this CTA's counts (read by the whole cluster)
+  uint32_t hist_tot[kBins1];    // the row's counts
+  uint32_t cand[kCandMax];      // this CTA's candidates (read by the whole cluster)
+  uint32_t all_cand[kCandMax];  // the cluster's candidates
+  uint32_t scan[kWarps];
+  uint32_t wgt[kWarps], weq[kWarps];  // per warp: keys > tau and == tau in its range, then their prefixes
+  uint32_t count;                     // this CTA's candidates
+  uint32_t cta_gt, cta_eq;            // this CTA's totals (read by later ranks)
+  uint32_t digit, above;
+};
+
+// Keys of row positions i .. i+3 (i a multiple of 4) that lie before `end`;
+// nv = how many do.  vec: the row is 16-byte aligned, so whole groups load
+// as one float4.
+__device__ __forceinline__ void load_keys4(const float *srow, int i, int end, bool vec, uint32_t (&k)[4],
+                                           int &nv) {
+  nv = min(max(end - i, 0), 4);
+  if (vec && nv == 4) {
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(srow + i));
+    k[0] = order_key(v.x);
+    k[1] = order_key(v.y);
+    k[2] = order_key(v.z);
+    k[3] = order_key(v.w);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k[j] = j < nv ? order_key(__ldcg(srow + i + j)) : 0u;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) topk_stream_kernel(const TopkParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  StreamShared &sh = *reinterpret_cast<StreamShared *>(smem_raw);
+  cg::cluster_group cl = cg::this_cluster();
+  pdl_launch_dependents();
+  const int C = static_cast<int>(cl.num_blocks());
+  const int q = static_cast<int>(cl.block_rank());
+  const int wr = blockIdx.x / C;  // row within the window
+  const int r = p.row_lo + wr;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = p.topk;
+  int32_t *out = p.topk_idx + static_cast<size_t>(r) * K;
+  int L = p.row_len[r];  // row metadata, not the indexer's output: read while it finishes
+  pdl_wait();            // the scores come from the indexer kernel
+  if (L < 0 || L > p.score_width) {
+    if (tid == 0 && q == 0) flag_status(p.status, DSA_DEV_BAD_ROW);
+    L = 0;
+  }
+  uint32_t *ghist = p.row_hist != nullptr ? p.row_hist + static_cast<size_t>(r) * kBins1 : nullptr;
+  if (L <= K) {  // every position is selected (same branch in every CTA of the cluster)
+    if (ghist != nullptr && q == 0)
+      for (int i = tid; i < kBins1; i += kThreads) ghist[i] = 0u;  // ready for the next step
+    const int per = (K + C - 1) / C;
+    for (int i = q * per + tid; i < min(K, (q + 1) * per); i += kThreads) out[i] = i < L ? i : -1;
+    return;
+  }
+  // this CTA's segment [lo, hi) and this warp's range [wlo, whi) of it
+  const int seg = (((L + C - 1) / C) + kStreamSegAlign - 1) / kStreamSegAlign * kStreamSegAlign;
+  const int lo = min(L, q * seg), hi = min(L, lo + seg);
+  const int ws = seg / kWarps;  // a multiple of kStreamStep
+  const int wlo = min(hi, lo + warp * ws), whi = min(hi, wlo + ws);
+  const float *srow = p.scores + static_cast<size_t>(wr) * p.score_width;
+  const bool vec = (p.score_width & 3) == 0;
+
+  // ---- A. the row's histogram
+  bool recount = ghist == nullptr;
+  if (!recount) {
+    uint32_t part = 0u;
+#pragma unroll
+    for (int j = 0; j < kBins1 / kThreads; ++j) {
+      const uint32_t v = __ldcg(ghist + j * kThreads + tid);
+      sh.hist_tot[j * kThreads + tid] = v;
+      part += v;
+    }
+    part = warp_sum(part);
+    if (lane == 0) sh.scan[warp] = part;
+  }
+  __syncthreads();
+  if (!recount) {
+    uint32_t total = 0u;
+#pragma unroll 8
+    for (int w = 0; w < kWarps; ++w) total += sh.scan[w];
+    recount = total != static_cast<uint32_t>(L);  // same verdict in every CTA
+  }
+  if (recount) {
+    for (int i = tid; i < kBins1; i += kThreads) sh.hist[i] = 0u;
+    __syncthreads();
+    for (int base = wlo; base < whi; base += kStreamStep) {
+      uint32_t k[kStreamU][4];
+      int nv[kStreamU];
+#pragma unroll
+      for (int u = 0; u < kStreamU; ++u) load_keys4(srow, base + u * 128 + 4 * lane, whi, vec, k[u], nv[u]);
+#pragma unroll
+      for (int u = 0; u < kStreamU; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nv[u]) atomicAdd(&sh.hist[k[u][j] >> 20], 1u);
+    }
+    __syncthreads();
+    cl.sync();
+    for (int b = tid; b < kBins1; b += kThreads) {
+      uint32_t s = 0u;
+      for (int rr = 0; rr < C; ++rr) s += cl.map_shared_rank(sh.hist, rr)[b];
+      sh.hist_tot[b] = s;
+    }
+  }
+  __syncthreads();
+
+  // ---- B. the bin of the k-th key
+  uint32_t need = static_cast<uint32_t>(K);
+  select_bin(sh, sh.hist_tot, kBins1, need);
+  const uint32_t d1 = min(sh.digit, static_cast<uint32_t>(kBins1 - 1));  // found whenever L > K
+  need -= sh.above;
+  const uint32_t in_bin = sh.hist_tot[d1];
+  uint32_t prefix = d1 << 20, mask = 0xFFF00000u;
+
+  // ---- C. the threshold key tau and how many keys equal to it still fit
+  if (in_bin <= static_cast<uint32_t>(kCandMax)) {
+    if (tid == 0) sh.count = 0u;
+    __syncthreads();
+    for (int base = wlo; base < whi; base += kStreamStep) {
+      uint32_t k[kStreamU][4];
+      int nv[kStreamU];
+#pragma unroll
+      for (int u = 0; u < kStreamU; ++u) load_keys4(srow, base + u * 128 + 4 * lane, whi, vec, k[u], nv[u]);
+#pragma unroll
+      for (int u = 0; u < kStreamU; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nv[u] && (k[u][j] & mask) == prefix) {
+            const uint32_t at = atomicAdd(&sh.count, 1u);  // order is irrelevant: only counts follow
+            if (at < static_cast<uint32_t>(kCandMax)) sh.cand[at] = k[u][j];
+          }
+    }
+    __syncthreads();
+    cl.sync();  // every CTA's candidates are complete (and the row histogram was read)
+    if (ghist != nullptr && q == 0)
+      for (int i = tid; i < kBins1; i += kThreads) ghist[i] = 0u;  // ready for the next step
+    uint32_t total = 0u;
+    for (int rr = 0; rr < C; ++rr) {
+      const uint32_t cnt = min(*cl.map_shared_rank(&sh.count, rr), static_cast<uint32_t>(kCandMax));
+      const uint32_t *src = cl.map_shared_rank(sh.cand, rr);
+      for (uint32_t i = tid; i < cnt && total + i < static_cast<uint32_t>(kCandMax); i += kThreads)
+        sh.all_cand[total + i] = src[i];
+      total += cnt;
+    }
+    if (tid == 0 && q == 0) {
+      if (total > static_cast<uint32_t>(kCandMax)) flag_status(p.status, DSA_DEV_BAD_ROW);  // scores vs histogram
+      if (total != in_bin) flag_status(p.status, DSA_DEV_BAD_HIST);
+    }
+    total = min(total, static_cast<uint32_t>(kCandMax));
+    __syncthreads();
+#pragma unroll 1
+    for (int shift = 10; shift >= 0; shift -= 10) {
+      const uint32_t dg = radix_pass(sh, sh.all_cand, total, shift, prefix, mask, need);
+      prefix |= dg << shift;
+      mask |= 0x3FFu << shift;
+    }
+  } else {
+    cl.sync();  // every CTA has read the row histogram
+    if (ghist != nullptr && q == 0)
+      for (int i = tid; i < kBins1; i += kThreads) ghist[i] = 0u;
+#pragma unroll 1
+    for (int shift = 10; shift >= 0; shift -= 10) {
+      cl.sync();  // nobody still reads this CTA's previous counts
+      for (int i = tid; i < kBins2; i += kThreads) sh.hist[i] = 0u;
+      __syncthreads();
+      for (int base = wlo; base < whi; base += kStreamStep) {
+        uint32_t k[kStreamU][4];
+        int nv[kStreamU];
+#pragma unroll
+        for (int u = 0; u < kStreamU; ++u) load_keys4(srow, base + u * 128 + 4 * lane, whi, vec, k[u], nv[u]);
+#pragma unroll
+        for (int u = 0; u < kStreamU; ++u)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j < nv[u] && (k[u][j] & mask) == prefix) atomicAdd(&sh.hist[(k[u][j] >> shift) & 0x3FFu], 1u);
+      }
+      __syncthreads();
+      cl.sync();
+      for (int b = tid; b < kBins2; b += kThreads) {
+        uint32_t s = 0u;
+        for (int rr = 0; rr < C; ++rr) s += cl.map_shared_rank(sh.hist, rr)[b];
+        sh.hist_tot[b] = s;
+      }
+      __syncthreads();
+      select_bin(sh, sh.hist_tot, kBins2, need);
+      const uint32_t dg = min(sh.digit, static_cast<uint32_t>(kBins2 - 1));  // found if the counts agree
+      if (tid == 0 && q == 0 && sh.digit >= static_cast<uint32_t>(kBins2)) flag_status(p.status, DSA_DEV_BAD_HIST);
+      need -= sh.above;
+      prefix |= dg << shift;
+      mask |= 0x3FFu << shift;
+    }
+  }
+  const uint32_t thr = prefix;  // tau
+
+  // ---- D. ranks of the selected keys in position order
+  {
+    uint32_t g = 0u, e = 0u;
+    for (int base = wlo; base < whi; base += kStreamStep) {
+      uint32_t k[kStreamU][4];
+      int nv[kStreamU];
+#pragma unroll
+      for (int u = 0; u < kStreamU; ++u) load_keys4(srow, base + u * 128 + 4 * lane, whi, vec, k[u], nv[u]);
+#pragma unroll
+      for (int u = 0; u < kStreamU; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nv[u]) {
+            g += k[u][j] > thr ? 1u : 0u;
+            e += k[u][j] == thr ? 1u : 0u;
+          }
+    }
+    g = warp_sum(g);
+    e = warp_sum(e);
+    if (lane == 0) {
+      sh.wgt[warp] = g;
+      sh.weq[warp] = e;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {  // exclusive prefixes over the warps, and the CTA's totals
+    uint32_t rg = 0u, re = 0u;
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t tg = sh.wgt[w], te = sh.weq[w];
+      sh.wgt[w] = rg;
+      sh.weq[w] = re;
+      rg += tg;
+      re += te;
+    }
+    sh.cta_gt = rg;
+    sh.cta_eq = re;
+  }
+  __syncthreads();
+  cl.sync();  // every CTA's totals are visible
+  uint32_t g = sh.wgt[warp], e = sh.weq[warp];
+  for (int rr = 0; rr < q; ++rr) {
+    g += *cl.map_shared_rank(&sh.cta_gt, rr);
+    e += *cl.map_shared_rank(&sh.cta_eq, rr);
+  }
+  for (int base = wlo; base < whi; base += kStreamStep) {
+    uint32_t k[kStreamU][4];
+    int nv[kStreamU];
+#pragma unroll
+    for (int u = 0; u < kStreamU; ++u) load_keys4(srow, base + u * 128 + 4 * lane, whi, vec, k[u], nv[u]);
+#pragma unroll
+    for (int u = 0; u < kStreamU; ++u) {
+      // this lane's four positions follow those of the lanes below it
+      uint32_t cg4 = 0u, ce4 = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < nv[u]) {
+          cg4 += k[u][j] > thr ? 1u : 0u;
+          ce4 += k[u][j] == thr ? 1u : 0u;
+        }
+      const uint32_t packed = (cg4 << 16) | ce4;
+      if (__any_sync(0xFFFFFFFFu, packed != 0u)) {  // most steps select nothing
+        const uint32_t incl = warp_incl_scan(packed, lane);
+        const uint32_t ex = incl - packed;
+        uint32_t gl = g + (ex >> 16), el = e + (ex & 0xFFFFu);
+        const int i0 = base + u * 128 + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (j >= nv[u]) continue;
+          if (k[u][j] > thr) {
+            const uint32_t o = gl + min(el, need);
+            if (o < static_cast<uint32_t>(K)) out[o] = i0 + j;
+            ++gl;
+          } else if (k[u][j] == thr) {
+            if (el < need && gl + el < static_cast<uint32_t>(K)) out[gl + el] = i0 + j;
+            ++el;
+          }
+        }
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        g += tot >> 16;
+        e += tot & 0xFFFFu;
+      }
+    }
+  }
+  cl.sync();  // keep this CTA's shared memory alive until the cluster is done with it
+}
+
 }  // namespace
 
 // CTAs per row: ceil(W / 16K), at most 4, keeps one row's chain short when
@@ -474,8 +786,18 @@ int topk_cluster_size(int score_width, int max_rows) {
 }
 
 cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, int rows, cudaStream_t st) {
+  if (cfg.score_width > kSegMax * kMaxCluster) {  // rows past what a cluster's shared memory holds
+    const size_t smem = sizeof(StreamShared);
+    cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(topk_stream_kernel, dim3(static_cast<unsigned>(rows * kStreamCluster)), dim3(kThreads), smem,
+                   st, static_cast<unsigned>(kStreamCluster), p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   const int C = topk_cluster_size(cfg.score_width, rows);
-  if (C > kMaxCluster) return cudaErrorInvalidValue;  // W <= 8 x 32K keys is checked on the host
+  if (C > kMaxCluster) return cudaErrorInvalidValue;
   const int seg_w = (((cfg.score_width + C - 1) / C) + 127) & ~127;
   if (seg_w > kSegMax) return cudaErrorInvalidValue;
   const int groups = (seg_w + 4 * kThreads - 1) / (4 * kThreads);

@@ -18,6 +18,13 @@ Five workloads, numbered by their seed:
                    score blocks of up to 4 rows, 1024 static row slots
   4  long fp8      B=16, lengths U{1024..131072}, indexer keys fp8 e4m3
                    with a per-token fp32 scale, top-k 2048
+  5  1M prefill    a 64-token prefill chunk at 1M (1,048,576) keys of
+                   context, one decode request just under 1M and one
+                   short decode request; score blocks of up to 4 rows,
+                   80 row slots, indexer 64x128 bf16, top-k 2048, 8 q /
+                   1 KV head, head dim 128 (the score-window case of a
+                   prefill chunk at 1M context, with one KV head so the
+                   caches stay a few GB)
 
 The problem statement these follow is Megatron-LM PR #7211 (DSA over GQA
 with paged KV caches): every query token is a row that routes to the top-k
@@ -100,6 +107,10 @@ WORKLOADS = [
         num_splits=19, max_rows=16, max_reqs=16, max_pages_per_req=2048,
         score_width=131072, block_rows=1, idx_key_dtype=KEY_FP8_E4M3,
         kind="decode"),
+    _wl("prefill64_at_1m", 5, num_q_heads=8, num_kv_heads=1, head_dim=128,
+        idx_heads=64, idx_dim=128, page_size=64, topk=2048, num_splits=4,
+        max_rows=80, max_reqs=3, max_pages_per_req=16384, score_width=1 << 20,
+        block_rows=4, idx_key_dtype=KEY_BF16, kind="mixed"),
 ]
 
 
@@ -224,6 +235,11 @@ def request_mix(wl: Workload):
     elif wl.seed == 4:
         cache_len = rng.integers(1024, 131072, size=16, endpoint=True).astype(np.int32)
         new = np.ones(16, dtype=np.int32)
+    elif wl.seed == 5:
+        near = int(rng.integers((1 << 20) - 4096, 1 << 20, endpoint=True))
+        short = int(rng.integers(4096, 65536, endpoint=True))
+        cache_len = np.array([near, 1 << 20, short], dtype=np.int32)
+        new = np.array([1, 64, 1], dtype=np.int32)
     else:
         raise ValueError(wl.seed)
     return cache_len, new

@@ -70,10 +70,13 @@ def _topk_cfg(dsa_lib, R, W_, K):
                                max_pages_per_req=(W_ + 63) // 64, score_width=W_, num_pages=1)
 
 
-# widths reach each cluster size: 1 CTA (300, 4096), 2 (32768), 4 (65536,
-# 131072) and 8 (262144, the longest row the top-k takes)
+# widths reach each cluster size of the in-shared-memory top-k: 1 CTA (300,
+# 4096), 2 (32768), 4 (65536, 131072) and 8 (262144, the longest row it
+# holds); past that the streaming top-k reads the score buffer in every
+# pass: 262148 and 1M / 4M keys (float4 loads), 262147 (a row stride that is
+# not a multiple of 4: scalar loads)
 @pytest.mark.parametrize("W_,K", [(4096, 512), (32768, 2048), (65536, 1024), (131072, 2048), (262144, 2048),
-                                  (300, 16)])
+                                  (300, 16), (262147, 300), (262148, 512), (1 << 20, 2048), (1 << 22, 2048)])
 def test_topk_crafted_rows(W_, K, dsa_lib, cuda_ok):
     rng = np.random.default_rng(W_ + K)
     R = 12

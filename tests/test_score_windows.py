@@ -83,11 +83,11 @@ def test_window_bounds_rejected_before_launch(lo, hi, dsa_lib):
 # ----------------------------------------------------------------------------
 # rows per window for each workload: edges that fall inside prefill score
 # blocks (mixed workload: blocks of 4 rows from row 48, edges at 250, 500...)
-_WINDOW_ROWS = {0: 1, 1: 3, 3: 250, 4: 5}
+_WINDOW_ROWS = {0: 1, 1: 3, 3: 250, 4: 5, 5: 16}
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("i", [0, 1, 3, 4])
+@pytest.mark.parametrize("i", [0, 1, 3, 4, 5])
 def test_windowed_step_identical(i, dsa_lib, cuda_ok):
     from sparse_attention_decode_paged_gb300.harness import DeviceStep
 
@@ -173,14 +173,18 @@ def test_window_calls_match_whole(i, windows, dsa_lib, cuda_ok):
 # sampled rows: on the mixed workload both sides of the window edge at row
 # 250, which cuts the prefill score block of rows 248..251, the edge at 500
 # (a block boundary), decode rows and pad rows; on the long fp8 workload
-# (5-row windows) every row
+# (5-row windows) every row; on the 1M-key prefill (16-row windows, 80 MB
+# of scores per window instead of 320 MB) the decode row near 1M keys, both
+# sides of the edges at rows 16 and 64 (inside the prefill blocks 13..16 and
+# 61..64), the short decode row and a pad row
 _ORACLE_ROWS = {3: [0, 23, 47, 48, 49, 246, 247, 248, 249, 250, 251, 252, 253, 498, 499, 500, 501, 558, 559, 560,
                     1023],
-                4: list(range(16))}
+                4: list(range(16)),
+                5: [0, 1, 15, 16, 17, 63, 64, 65, 66]}
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("i", [3, 4])
+@pytest.mark.parametrize("i", [3, 4, 5])
 def test_windowed_step_vs_oracle(i, dsa_lib, cuda_ok):
     """A step with a score budget (several row windows) compared with the
     oracle: each window's scores within the score tolerance, its top-k
