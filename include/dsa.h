@@ -137,7 +137,16 @@ enum {
    * The sparse attention then moves each selected token with one copy
    * instead of two; results are identical to the separate layout.  A layout
    * of this library's own (the pages keep K and V apart). */
-  DSA_FLAG_KV_INTERLEAVED = 1 << 1
+  DSA_FLAG_KV_INTERLEAVED = 1 << 1,
+  /* Test only: exercises the bounded-wait failure path without a fault.  The
+   * lightning indexer's MMA thread first waits on a barrier that nothing
+   * completes, with a budget of about 1 ms instead of the usual ~1 s; the wait
+   * runs out, the kernel sets DSA_DEV_TIMEOUT and its abort flag, every role
+   * leaves its loop (the producer still waits for its copies in flight), the
+   * launch returns and the scores are incomplete.  The next call without the
+   * bit runs normally once the status word is reset.  Never set it outside a
+   * test. */
+  DSA_FLAG_TEST_WAIT_TIMEOUT = 1 << 2
 };
 
 /* Every pointer one fused step needs (all device pointers). */

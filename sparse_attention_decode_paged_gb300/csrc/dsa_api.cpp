@@ -147,7 +147,8 @@ dsa_status_t dsa_validate_config(const dsa_config_t *c) {
     return fail(DSA_ERR_INVALID_ARG, "idx_key_dtype %d unknown", c->idx_key_dtype);
   if (!(c->sm_scale > 0.f) || !std::isfinite(c->sm_scale))
     return fail(DSA_ERR_INVALID_ARG, "sm_scale must be positive and finite");
-  if ((c->flags & ~static_cast<int32_t>(DSA_FLAG_TOPK_HISTOGRAM | DSA_FLAG_KV_INTERLEAVED)) != 0)
+  if ((c->flags & ~static_cast<int32_t>(DSA_FLAG_TOPK_HISTOGRAM | DSA_FLAG_KV_INTERLEAVED |
+                                        DSA_FLAG_TEST_WAIT_TIMEOUT)) != 0)
     return fail(DSA_ERR_INVALID_ARG, "unknown flags 0x%x", c->flags);
   if (static_cast<long long>(c->max_reqs) * c->max_pages_per_req > 0x7FFFFFFFLL)
     return fail(DSA_ERR_INVALID_ARG, "page table larger than 2^31 entries");
@@ -332,6 +333,7 @@ dsa_status_t indexer_impl(const dsa_config_t *cfg, int32_t row_begin, int32_t ro
   p.row_hist = hist ? key_hist_of(cfg, workspace) : nullptr;
   p.row_lo = row_begin;
   p.row_hi = row_end;
+  p.test_timeout = (cfg->flags & DSA_FLAG_TEST_WAIT_TIMEOUT) != 0 ? 1 : 0;
   return cuda_status(dsa::launch_indexer_tc(*cfg, p, stream), "indexer launch");
 }
 

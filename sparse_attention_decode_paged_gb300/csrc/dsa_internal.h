@@ -24,6 +24,7 @@ struct IndexerParams {
   int32_t idx_heads, idx_dim, max_rows, max_reqs, max_pages_per_req, score_width, num_pages;
   int32_t page_size, block_rows;
   int32_t row_lo, row_hi;   // the row window scored (0, max_rows for all rows)
+  int32_t test_timeout;     // DSA_FLAG_TEST_WAIT_TIMEOUT: one wait that nothing completes
 };
 
 struct TopkParams {

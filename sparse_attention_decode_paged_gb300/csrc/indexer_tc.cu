@@ -52,6 +52,7 @@ constexpr int kTok = 128;  // tokens per key tile (MMA M)
 constexpr int kWarps = 10;  // 0 producer, 1 MMA, 2..5 and 6..9 two epilogue warpgroups
 constexpr int kThreads = kWarps * 32;
 constexpr long long kWaitBudget = 2000000000LL;  // SM cycles (about 1 s)
+constexpr long long kTestWaitBudget = 2000000LL;  // SM cycles (about 1 ms): the test-only wait
 constexpr int kMaxRowsTc = 4096;                  // prefix table capacity
 constexpr int kMaxStages = 16;                    // key-tile ring depth at most
 
@@ -539,7 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t ad_s = adesc0, bd_q = 0;
       uint32_t d = tmem, idesc = 0;
       bool any = false;
-      for (; wk.valid(); wk.next()) {
+      // test only: a wait on the MMA-completion barrier before any MMA is
+      // issued, which nothing completes, so it runs out after a short budget
+      const bool test_stop = p.test_timeout != 0 && !tc::mbar_wait(DONE, 0, abort_flag, kTestWaitBudget);
+      for (; wk.valid() && !test_stop; wk.next()) {
         const int s = ms, ab = ma;
         if (wk.block != cur) {
           cur = wk.block;

@@ -37,6 +37,7 @@ DSA_KEY_FP8_E4M3 = 1
 
 DSA_FLAG_TOPK_HISTOGRAM = 1 << 0
 DSA_FLAG_KV_INTERLEAVED = 1 << 1
+DSA_FLAG_TEST_WAIT_TIMEOUT = 1 << 2  # test only: one indexer wait runs out (see dsa.h)
 
 EXPORTED = (
     "dsa_validate_config", "dsa_workspace_size", "dsa_workspace_layout",

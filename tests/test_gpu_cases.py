@@ -391,3 +391,53 @@ def test_kv_interleaved_layout_identical(i, dsa_lib, cuda_ok):
     dsa_lib.dsa_merge(cfg, v["part_m"], v["part_l"], v["part_acc"], t["out"], t["lse"])
     torch.cuda.synchronize()
     assert torch.equal(sep.t["out"], itl.t["out"])
+
+
+# ----------------------------------------------------------------------------
+# the bounded-wait failure path, without a fault
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("i", [0, 4])
+def test_wait_that_runs_out_flags_timeout_and_the_next_step_is_clean(i, dsa_lib, cuda_ok):
+    """With the test-only flag the indexer's MMA thread waits on a barrier
+    that nothing completes, with a ~1 ms budget: the wait runs out, the
+    kernel sets DSA_DEV_TIMEOUT, every role leaves its loop (the producer
+    still waits for its copies in flight) and the launch returns well within
+    a second.  The context stays usable: after resetting the status word, a
+    step without the flag gives the same result as before (bf16 keys and
+    fp8 keys, whose epilogue path differs)."""
+    import time
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    inp = W.generate(i, with_kv=True)
+    dev = DeviceStep(inp)
+    dev.step()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    ref_out, ref_lse = dev.t["out"].clone(), dev.t["lse"].clone()
+    ref_scores = dev.views["scores"].clone()
+
+    t = dev.t
+    cfg = dsa_lib.config_from_workload(inp["workload"], inp["num_pages"],
+                                       flags=dev.cfg.flags | dsa_lib.DSA_FLAG_TEST_WAIT_TIMEOUT)
+    dsa_lib.dsa_validate_config(cfg)
+    scores = torch.full_like(dev.views["scores"], 7.0)
+    t0 = time.perf_counter()
+    dsa_lib.dsa_indexer_scores(cfg, t["q_idx"], t["w"], t["idx_cache"], t["idx_scale"], t["page_table"],
+                               t["row_req"], t["row_len"], t["block_first"], t["block_nrows"], scores,
+                               dev.workspace)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    status = dev.status()
+    assert status & dsa_lib.DSA_DEV_TIMEOUT, hex(status)
+    assert status == dsa_lib.DSA_DEV_TIMEOUT, hex(status)  # nothing else went wrong
+    assert elapsed < 0.5, elapsed  # the ~1 ms wait, not the ~1 s one
+    assert (scores == 7.0).all()   # no MMA ran, so no score was written
+
+    dsa_lib.dsa_reset_device_status(dev.workspace)
+    dev.t["out"].zero_()
+    dev.step()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    assert torch.equal(dev.views["scores"], ref_scores)
+    assert torch.equal(dev.t["out"].view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(dev.t["lse"], ref_lse)

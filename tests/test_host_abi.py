@@ -58,7 +58,7 @@ def test_validate_config_accepts_all_workloads(dsa_lib):
     (dict(topk=0), 1), (dict(topk=40000), 1), (dict(score_width=40000), 1),
     (dict(num_splits=0), 2), (dict(block_rows=5), 2), (dict(idx_key_dtype=7), 1),
     (dict(sm_scale=-1.0), 1), (dict(sm_scale=float("inf")), 1), (dict(max_rows=0), 1),
-    (dict(flags=6), 1),
+    (dict(flags=8), 1),
 ])
 def test_validate_config_rejects(dsa_lib, bad, status):
     cfg = _cfg(dsa_lib, **bad)
