@@ -178,6 +178,8 @@ typedef struct {
   size_t part_m;    /* fp32 [max_rows, num_q_heads, num_splits]           */
   size_t part_l;    /* fp32 [max_rows, num_q_heads, num_splits]           */
   size_t part_acc;  /* fp32 [max_rows, num_q_heads, num_splits, head_dim] */
+  size_t group;     /* prefill-group scratch (see dsa_sparse_attn); empty
+                     * (= key_hist) when the config has no prefill groups  */
   size_t key_hist;  /* uint32 [max_rows, 4096]: score-key histograms (zero between steps) */
   size_t total;     /* bytes to allocate (256-byte aligned regions)       */
 } dsa_workspace_layout_t;
@@ -213,8 +215,13 @@ dsa_status_t dsa_score_windows(const dsa_config_t *cfg, int32_t *window_rows, in
  *   S4  = round(4 * C / max_rows)           (about four programs per CTA)
  *   S1  = max(1, floor(C / max_rows))       (one wave of programs)
  *   S   = S4 <= cap ? max(1, S4) : min(cap, S1)
+ * and, when the config has prefill row groups (see dsa_sparse_attn), whose
+ * programs are (16-row slot, KV head, split) on one CTA per SM,
+ *   S   = max(S, min(cap, max(1, floor(16 * num_sms / (slots * num_kv_heads)))))
+ * with slots = ceil(max_rows / 16) (about 8 programs per CTA when half the
+ * slots form groups).
  * e.g. on 152 SMs: 64 rows, top-k 2048 -> 19; 8 rows, top-k 512 -> 16;
- * 16 rows -> 19; 1024 rows -> 1.
+ * 16 rows -> 19; 1024 rows -> 1, or 4 with prefill groups and 8 KV heads.
  * Errors: DSA_ERR_INVALID_ARG (bad config, NULL), DSA_ERR_CUDA (num_sms <= 0
  * and no device to query).
  */
@@ -340,6 +347,26 @@ dsa_status_t dsa_topk_window(const dsa_config_t *cfg, int32_t row_begin, int32_t
  * part_m, part_l: device fp32 [max_rows, num_q_heads, num_splits];
  * part_acc: device fp32 [max_rows, num_q_heads, num_splits, head_dim].
  */
+/*
+ * Prefill row groups (commit message 5: a group of consecutive prefill
+ * tokens attends to the union of the group's selected keys with a per-token
+ * mask).  When block_rows > 1, num_q_heads == 8 * num_kv_heads and head_dim
+ * == 128, each slot of 16 consecutive rows [16i, 16i + 16) whose most common
+ * request has at least 8 rows there is considered: if their longest row is
+ * at most min(score_width, 64 * topk) rounded up to 128 positions long and
+ * the union of their selections fills at least a quarter of it, those rows
+ * form a group and their attention runs on the tensor cores over the union,
+ * each row masked to its own selection, computing the same partial state as
+ * the per-row path: probabilities in fp32, carried into the value product as
+ * two bf16 terms whose sum is the fp32 value to about 2^-17 relative, and m
+ * the exact maximum.  For a group row, split s covers the positions in the tiles
+ * [s*T/S, (s+1)*T/S) of the T tiles of 128 positions ([128i, 128i + 128))
+ * that hold a position some group row selected, in ascending order; the
+ * row's partial state for split s is over its own selected positions in
+ * those tiles (an empty share gives the empty state).  Every other row
+ * splits its top-k slots as above.  The union lives in the workspace's
+ * `group` region.
+ */
 dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void *k_cache,
                              const void *v_cache, const int32_t *page_table,
                              const int32_t *row_req, const int32_t *row_len,
@@ -409,7 +436,9 @@ const char *dsa_last_error(void);
 
 /* Library version string.  0.2: dsa_config_t gained score_buffer_bytes
  * (its size changed; rebuild callers), and the _window calls,
- * dsa_score_windows and dsa_suggest_num_splits were added. */
+ * dsa_score_windows and dsa_suggest_num_splits were added.  0.3:
+ * dsa_workspace_layout_t gained `group` (its size changed), prefill row
+ * groups attend on the tensor cores, score_width may reach 4194304. */
 const char *dsa_version(void);
 
 #ifdef __cplusplus

@@ -199,6 +199,12 @@ __device__ __forceinline__ RowSplit row_split(const AttnParams &p, int item, boo
   RowSplit x;
   x.r = item / p.num_splits;
   x.s = item % p.num_splits;
+  if (p.grouped != nullptr && p.grouped[x.r] != 0) {  // the prefill-group kernel has this row
+    x.L = -1;
+    x.req = 0;
+    x.a = x.b = 0;
+    return x;
+  }
   int L = p.row_len[x.r];
   const int req = p.row_req[x.r];
   const bool ok = L >= 0 && L <= p.score_width && (L == 0 || (req >= 0 && req < p.max_reqs));
@@ -329,7 +335,9 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
   }
   pdl_launch_dependents();
   // this CTA's items from the row metadata (not produced by the top-k, so
-  // read while the top-k still runs)
+  // read while the top-k still runs; with prefill groups the rows the group
+  // kernel takes are known only after the kernels before)
+  if (p.grouped != nullptr) pdl_wait();
   const int items = p.max_rows_attn * S;
   const int nmine = static_cast<int>(blockIdx.x) < items ? (items - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
   const int ncache = min(nmine, kItemCache);
@@ -339,7 +347,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     *reinterpret_cast<int4 *>(item_tab + 8 * k) = make_int4(x.a, x.b, x.L, x.req);
     *reinterpret_cast<int2 *>(item_tab + 8 * k + 4) = make_int2(x.r, x.s);
   }
-  pdl_wait();  // the selection comes from the top-k kernel
+  if (p.grouped == nullptr) pdl_wait();  // the selection comes from the top-k kernel
   __syncthreads();
 
   const long long tok_stride = static_cast<long long>(Hkv) * D * (p.kv_interleaved ? 2 : 1);  // elements per token
@@ -409,6 +417,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     int cst = 0, cph = 0;  // ring stage and phase of the next chunk
     for (int k = 0; k < nmine; ++k) {
       const RowSplit x = item_split(p, item_tab, ncache, k, false);
+      if (x.L < 0) continue;  // a prefill-group row: its partials come from the group kernel
       // A operand: this group's query heads (rows 8..15 are zero padding)
       uint32_t qa[D / 16][2];
 #pragma unroll

@@ -88,6 +88,15 @@ dsa_status_t layout_of(const dsa_config_t *c, dsa_workspace_layout_t *l) {
   off = align256(off + R * HS * sizeof(float));
   l->part_acc = off;
   off = align256(off + R * HS * c->head_dim * sizeof(float));
+  l->group = off;
+  if (dsa::group_path_enabled(*c)) {  // grouped flags, union counts, positions, masks
+    const size_t nslots = (R + dsa::kGroupRows - 1) / dsa::kGroupRows;
+    const size_t umax = static_cast<size_t>(dsa::group_union_capacity(*c));
+    off = align256(off + R * sizeof(int32_t));
+    off = align256(off + nslots * sizeof(int32_t));
+    off = align256(off + nslots * (umax / 128) * sizeof(int32_t));
+    off = align256(off + nslots * umax * sizeof(uint16_t));
+  }
   l->key_hist = off;
   off = align256(off + R * 4096 * sizeof(uint32_t));
   l->total = off;
@@ -95,6 +104,27 @@ dsa_status_t layout_of(const dsa_config_t *c, dsa_workspace_layout_t *l) {
 }
 
 uint32_t *status_word(void *workspace) { return static_cast<uint32_t *>(workspace); }
+
+// Pointers into the prefill-group scratch of a workspace (the config uses
+// the group path).
+dsa::GroupParams group_params(const dsa_config_t *c, void *workspace) {
+  dsa_workspace_layout_t l;
+  layout_of(c, &l);
+  char *g = static_cast<char *>(workspace) + l.group;
+  const size_t R = static_cast<size_t>(c->max_rows);
+  dsa::GroupParams gp;
+  gp.nslots = static_cast<int32_t>((R + dsa::kGroupRows - 1) / dsa::kGroupRows);
+  gp.umax = dsa::group_union_capacity(*c);
+  size_t off = 0;
+  gp.grouped = reinterpret_cast<int32_t *>(g + off);
+  off = align256(off + R * sizeof(int32_t));
+  gp.ntiles = reinterpret_cast<int32_t *>(g + off);
+  off = align256(off + gp.nslots * sizeof(int32_t));
+  gp.tiles = reinterpret_cast<int32_t *>(g + off);
+  off = align256(off + static_cast<size_t>(gp.nslots) * (gp.umax / 128) * sizeof(int32_t));
+  gp.umask = reinterpret_cast<uint32_t *>(g + off);
+  return gp;
+}
 
 }  // namespace
 
@@ -199,7 +229,15 @@ dsa_status_t dsa_suggest_num_splits(const dsa_config_t *cfg, int32_t num_sms, in
   const long long cap = std::min<long long>(64, std::max(1, cfg->topk / 32));
   const long long s4 = (4 * C + R / 2) / R;
   const long long s1 = std::max<long long>(1, C / R);
-  *num_splits = static_cast<int32_t>(s4 <= cap ? std::max<long long>(1, s4) : std::min(cap, s1));
+  long long S = s4 <= cap ? std::max<long long>(1, s4) : std::min(cap, s1);
+  if (dsa::group_path_enabled(*cfg)) {
+    // prefill row groups run one program per (slot, KV head, split) on one
+    // CTA per SM: about 8 programs per CTA when half the slots form groups
+    const long long slots = (R + dsa::kGroupRows - 1) / dsa::kGroupRows;
+    const long long sg = (16LL * num_sms) / (slots * cfg->num_kv_heads);
+    S = std::max(S, std::min(cap, std::max<long long>(1, sg)));
+  }
+  *num_splits = static_cast<int32_t>(S);
   return ok();
 }
 
@@ -445,6 +483,16 @@ dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void 
   p.kv_interleaved = kv_interleaved ? 1 : 0;
   p.page_shift = 0;
   while ((1 << p.page_shift) < cfg->page_size) ++p.page_shift;  // page_size is a validated power of two
+  p.grouped = nullptr;
+  if (dsa::group_path_enabled(*cfg)) {
+    // prefill row groups: the union, their tensor-core attention, then the
+    // other rows (the decode kernel leaves the grouped rows alone)
+    const dsa::GroupParams gp = group_params(cfg, workspace);
+    p.grouped = gp.grouped;
+    cudaError_t e = dsa::launch_group_union(*cfg, p, gp, stream);
+    if (e == cudaSuccess) e = dsa::launch_group_attn(*cfg, p, gp, stream);
+    if (e != cudaSuccess) return cuda_status(e, "prefill-group attention launch");
+  }
   return cuda_status(dsa::launch_sparse_attn(*cfg, p, stream), "sparse attention launch");
 }
 
@@ -503,6 +551,6 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *a, void *w
 
 const char *dsa_last_error(void) { return g_last_error.c_str(); }
 
-const char *dsa_version(void) { return "dsa-gb300 0.2 (sm_103a)"; }
+const char *dsa_version(void) { return "dsa-gb300 0.3 (sm_103a)"; }
 
 }  // extern "C"

@@ -54,6 +54,22 @@ struct AttnParams {
   float sm_scale_log2;     // sm_scale * log2(e)
   int32_t kv_interleaved;  // 1: one copy moves a token's K and V rows
   int32_t page_shift;      // log2(page_size)
+  const int32_t *grouped;  // [R] 1: the row is attended by the prefill-group kernel (null: no groups)
+};
+
+// Prefill row groups: the rows of one request in a slot of kGroupRows
+// consecutive rows (at least kGroupMin of them) attend to the union of their
+// selections on the tensor cores (group_attn.cu).
+constexpr int kGroupRows = 16;
+constexpr int kGroupMin = 8;
+
+struct GroupParams {
+  int32_t *grouped;  // [R] 1: the row is a group member
+  int32_t *ntiles;   // [nslots] 128-position tiles holding a selected position (0: the slot is no group)
+  int32_t *tiles;    // [nslots, umax / 128] those tiles' indices, ascending
+  uint32_t *umask;   // [nslots, umax / 128, 16, 4] per tile and slot row j: bit b of word w set if
+                     // row j selected position 128 * tile + 32 * w + b
+  int32_t umax, nslots;  // umax: positions a group may span (a multiple of 128)
 };
 
 struct MergeParams {
@@ -99,5 +115,11 @@ cudaError_t launch_indexer_tc(const dsa_config_t &cfg, const IndexerParams &p, c
 cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, int rows, cudaStream_t st);
 cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cudaStream_t st);
 cudaError_t launch_merge(const dsa_config_t &cfg, const MergeParams &p, cudaStream_t st);
+// The prefill-group path: whether a config uses it, the union capacity per
+// slot (positions, a multiple of 128), and its two kernels.
+bool group_path_enabled(const dsa_config_t &cfg);
+int32_t group_union_capacity(const dsa_config_t &cfg);
+cudaError_t launch_group_union(const dsa_config_t &cfg, const AttnParams &p, const GroupParams &gp, cudaStream_t st);
+cudaError_t launch_group_attn(const dsa_config_t &cfg, const AttnParams &p, const GroupParams &gp, cudaStream_t st);
 
 }  // namespace dsa

@@ -72,7 +72,7 @@ class dsa_step_args_t(ctypes.Structure):
 
 class dsa_workspace_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "status", "scores", "topk_idx", "part_m", "part_l", "part_acc", "key_hist", "total")]
+        "status", "scores", "topk_idx", "part_m", "part_l", "part_acc", "group", "key_hist", "total")]
 
 
 def _load():

@@ -100,7 +100,7 @@ WORKLOADS = [
         score_width=32768, block_rows=1, idx_key_dtype=KEY_BF16, kind="decode"),
     _wl("mixed_48dec_512prefill", 3, num_q_heads=64, num_kv_heads=8,
         head_dim=128, idx_heads=64, idx_dim=128, page_size=64, topk=2048,
-        num_splits=1, max_rows=1024, max_reqs=49, max_pages_per_req=512,
+        num_splits=4, max_rows=1024, max_reqs=49, max_pages_per_req=512,
         score_width=32768, block_rows=4, idx_key_dtype=KEY_BF16, kind="mixed"),
     _wl("long_fp8_b16_l1024_131072", 4, num_q_heads=64, num_kv_heads=8,
         head_dim=128, idx_heads=64, idx_dim=128, page_size=64, topk=2048,

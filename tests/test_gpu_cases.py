@@ -441,3 +441,90 @@ def test_wait_that_runs_out_flags_timeout_and_the_next_step_is_clean(i, dsa_lib,
     assert torch.equal(dev.views["scores"], ref_scores)
     assert torch.equal(dev.t["out"].view(torch.int16), ref_out.view(torch.int16))
     assert torch.equal(dev.t["lse"], ref_lse)
+
+
+# ----------------------------------------------------------------------------
+# prefill row groups (tensor-core attention over the union of a group's
+# selections)
+# ----------------------------------------------------------------------------
+def _group_slots(row_req, row_len, idx, wl):
+    """The grouping rule the library states: in each slot of 16 rows, the
+    rows of the request with the most rows there (ties: the lowest row's),
+    if there are at least 8, their longest row spans at most
+    min(score_width, 64 * topk) rounded up to 128 positions, and their union
+    of selected positions fills at least a quarter of it."""
+    umax = -(-min(wl.score_width, 64 * wl.topk) // 128) * 128
+    groups = {}
+    for slot in range((wl.max_rows + 15) // 16):
+        rows = [r for r in range(16 * slot, min(16 * slot + 16, wl.max_rows)) if row_len[r] > 0]
+        if not rows:
+            continue
+        counts = {}
+        for r in rows:
+            counts.setdefault(int(row_req[r]), []).append(r)
+        best = max(counts.values(), key=lambda rs: (len(rs), -rs[0]))
+        lmax = max(int(row_len[r]) for r in best)
+        if len(best) < 8 or lmax > umax:
+            continue
+        union = np.unique(np.concatenate([idx[r][idx[r] >= 0] for r in best]))
+        if 4 * union.size >= lmax:
+            groups[slot] = (best, union)
+    return groups
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_prefill_groups_vs_oracle(splits, dsa_lib, cuda_ok):
+    """The mixed step's prefill rows go through the group kernel: their
+    outputs match the oracle on their own selections, and each split's
+    partial state matches the oracle over the row's selected positions in
+    that split's union tiles; the decode rows keep the slot splits."""
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    inp = W.generate(3)
+    wl = inp["workload"]
+    dev = DeviceStep(inp, num_splits=splits, flags=dsa_lib.DSA_FLAG_KV_INTERLEAVED)
+    dev.step()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+    idx = dev.views["topk_idx"].cpu().numpy()
+    groups = _group_slots(rows["row_req"], rows["row_len"], idx, wl)
+    assert len(groups) == 32 and all(len(m) == 16 for m, _ in groups.values())  # rows 48..559
+    lay = dsa_lib.dsa_workspace_layout(dev.cfg)
+    grouped = dev.workspace[lay["group"]:lay["group"] + 4 * wl.max_rows].view(torch.int32).cpu().numpy()
+    want_grouped = np.zeros(wl.max_rows, np.int32)
+    for m, _ in groups.values():
+        want_grouped[m] = 1
+    assert np.array_equal(grouped, want_grouped)
+
+    out = dev.t["out"].float().cpu().numpy().astype(np.float64)
+    pm = dev.views["part_m"].cpu().numpy().astype(np.float64)
+    pl = dev.views["part_l"].cpu().numpy().astype(np.float64)
+    pa = dev.views["part_acc"].cpu().numpy().astype(np.float64)
+    q = O.bf16_bits_to_f64(inp["q"])
+    for slot in sorted(groups)[::5] + [max(groups)]:
+        members, union = groups[slot]
+        tiles = np.unique(union // 128)  # the 128-position tiles holding a selected position
+        T = tiles.size
+        for r in members[::5] + [members[-1]]:
+            sel = idx[r][idx[r] >= 0]
+            k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel)
+            o, _ = O.attention_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads)
+            np.testing.assert_allclose(out[r], o, atol=1e-2, rtol=2e-2, err_msg=f"row {r}")
+            for s in range(splits):
+                mine = tiles[s * T // splits:(s + 1) * T // splits]
+                part = sel[np.isin(sel // 128, mine)]
+                k, v = O.kv_rows(inp, int(rows["row_req"][r]), part)
+                m, l, acc = O.split_partials_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads, 1)
+                fin = np.isfinite(m[:, 0])
+                assert np.array_equal(fin, np.isfinite(pm[r, :, s])), (r, s)
+                assert (pl[r, ~fin, s] == 0).all() and (pa[r, ~fin, s] == 0).all(), (r, s)
+                np.testing.assert_allclose(pm[r, fin, s], m[fin, 0], atol=1e-2, rtol=2e-2, err_msg=f"m {r} {s}")
+                np.testing.assert_allclose(pl[r, fin, s], l[fin, 0], rtol=2e-2, atol=0, err_msg=f"l {r} {s}")
+                np.testing.assert_allclose(pa[r, fin, s] / pl[r, fin, s][:, None], acc[fin, 0] / l[fin, 0][:, None],
+                                           atol=1e-2, rtol=2e-2, err_msg=f"acc/l {r} {s}")
+    for r in (0, 23, 47):  # decode rows
+        sel = idx[r][idx[r] >= 0]
+        k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel)
+        o, _ = O.attention_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads)
+        np.testing.assert_allclose(out[r], o, atol=1e-2, rtol=2e-2, err_msg=f"row {r}")

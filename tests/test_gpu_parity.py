@@ -168,7 +168,39 @@ def test_attention_vs_oracle_on_gpu_selection(problem):
         np.testing.assert_allclose(lse[r], ls, atol=ATOL_OUT, rtol=RTOL_OUT, err_msg=f"row {r}")
 
 
-def test_split_partials_vs_oracle(problem):
+def _grouped_rows(dev, dsa_lib):
+    """Rows the library put into prefill row groups (its `group` region)."""
+    R = dev.cfg.max_rows
+    lay = dsa_lib.dsa_workspace_layout(dev.cfg)
+    if lay["group"] == lay["key_hist"]:  # the config has no prefill groups
+        return np.zeros(R, bool)
+    return dev.workspace[lay["group"]:lay["group"] + 4 * R].view(torch.int32).cpu().numpy() != 0
+
+
+def _group_row_partials(inp, rows, idx, grouped, q, r):
+    """Oracle partial state of group row r: split s covers the tiles
+    [s*T/S, (s+1)*T/S) of the T 128-position tiles holding a position some
+    row of its group (the grouped rows of its 16-row slot) selected, and the
+    row's state there is over its own selected positions in those tiles."""
+    wl = inp["workload"]
+    S = wl.num_splits
+    slot = r // 16
+    members = [j for j in range(16 * slot, 16 * slot + 16) if grouped[j]]
+    union = np.unique(np.concatenate([idx[j][idx[j] >= 0] for j in members]))
+    tiles = np.unique(union // 128)
+    T = tiles.size
+    sel = idx[r][idx[r] >= 0]
+    Hq, D = wl.num_q_heads, wl.head_dim
+    m, l, acc = np.full((Hq, S), -np.inf), np.zeros((Hq, S)), np.zeros((Hq, S, D))
+    for s in range(S):
+        part = sel[np.isin(sel // 128, tiles[s * T // S:(s + 1) * T // S])]
+        k, v = O.kv_rows(inp, int(rows["row_req"][r]), part)
+        ms, ls, accs = O.split_partials_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads, 1)
+        m[:, s], l[:, s], acc[:, s] = ms[:, 0], ls[:, 0], accs[:, 0]
+    return m, l, acc
+
+
+def test_split_partials_vs_oracle(problem, dsa_lib):
     i, inp, dev = problem
     wl = inp["workload"]
     rows = _rows(inp)
@@ -180,11 +212,15 @@ def test_split_partials_vs_oracle(problem):
     sample = _sample(i, rows)
     if len(sample) > 48:  # spread the split checks over the sample
         sample = sample[::max(1, len(sample) // 48)]
+    grouped = _grouped_rows(dev, dsa_lib)
     for r in sample:
         L = int(rows["row_len"][r])
         sel = idx[r][idx[r] >= 0]
-        k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel) if L else (np.zeros((0, wl.num_kv_heads, wl.head_dim)),) * 2
-        m, l, acc = O.split_partials_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads, wl.num_splits)
+        if grouped[r]:
+            m, l, acc = _group_row_partials(inp, rows, idx, grouped, q, r)
+        else:
+            k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel) if L else (np.zeros((0, wl.num_kv_heads, wl.head_dim)),) * 2
+            m, l, acc = O.split_partials_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads, wl.num_splits)
         fin = np.isfinite(m)
         assert np.array_equal(fin, np.isfinite(pm[r])), r
         # empty splits: l = 0 and acc = 0 exactly

@@ -122,7 +122,7 @@ def test_workspace_layout(dsa_lib):
     cfg = _cfg(dsa_lib)
     lay = dsa_lib.dsa_workspace_layout(cfg)
     assert lay["status"] == 0
-    order = ["status", "scores", "topk_idx", "part_m", "part_l", "part_acc", "key_hist", "total"]
+    order = ["status", "scores", "topk_idx", "part_m", "part_l", "part_acc", "group", "key_hist", "total"]
     offs = [lay[k] for k in order]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lay["topk_idx"] - lay["scores"] >= 64 * 32768 * 4
