@@ -73,7 +73,8 @@ constexpr int kGWarps = 10;                       // producer, MMA, 2 softmax wa
 constexpr int kGThreads = kGWarps * 32;
 constexpr long long kGWaitBudget = 2000000000LL;  // SM cycles (about 1 s)
 constexpr int kUnionThreads = 512;
-constexpr int kUnionChunk = 8192;                 // positions per bitmask chunk
+constexpr int kUnionSpan = 32768;                 // positions per pass (bitmasks in shared memory)
+constexpr int kUnionScan = 8192;                  // positions per scan step (16 per thread)
 constexpr float kLn2G = 0.69314718055994530942f;
 
 // tensor-memory columns, per softmax warpgroup w: S_w [128 x 128] fp32 at
@@ -117,11 +118,11 @@ __device__ __forceinline__ SlotInfo slot_members(const AttnParams &p, int slot, 
 }
 
 __global__ void __launch_bounds__(kUnionThreads) group_union_kernel(const AttnParams p, const GroupParams gp) {
-  __shared__ uint32_t mask2[kUnionChunk / 2];  // two 16-bit row masks per word
+  extern __shared__ uint32_t mask2[];          // kUnionSpan / 2 words: two 16-bit row masks per word
   __shared__ uint32_t wsum[kUnionThreads / 32];
   __shared__ uint32_t wtiles[kUnionThreads / 32];  // per warp: its 4 tiles that hold a selected position
   __shared__ int s_info[4];                    // members, req, lmax, n
-  __shared__ int s_rng[kGroupRows][2];         // each member's selected entries inside the chunk
+  __shared__ int s_n[kGroupRows], s_len[kGroupRows];  // each member's selected entries and length
   pdl_launch_dependents();
   const int slot = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (warp == 0) {
@@ -141,120 +142,103 @@ __global__ void __launch_bounds__(kUnionThreads) group_union_kernel(const AttnPa
   const int tmax = gp.umax / kGT;
   int *tiles_out = gp.tiles + static_cast<size_t>(slot) * tmax;
   uint32_t *msk_out = gp.umask + static_cast<size_t>(slot) * (gp.umax / kGT) * 64;
+  if (tid < kGroupRows) {
+    const bool mem = (members >> tid) & 1u;
+    const int L = mem ? p.row_len[slot * kGroupRows + tid] : 0;
+    s_len[tid] = L;
+    s_n[tid] = mem ? min(p.topk, L) : 0;
+  }
   pdl_wait();  // the selection comes from the top-k kernel
+  __syncthreads();
   const int32_t *pt = p.page_table + static_cast<size_t>(max(req, 0)) * p.max_pages_per_req;
+  const int K = p.topk;
   int ntile = 0, total = 0;  // tiles holding a selected position, selected positions
-  for (int c0 = 0; c0 < lmax && members != 0u; c0 += kUnionChunk) {
-    for (int i = tid; i < kUnionChunk / 2; i += kUnionThreads) mask2[i] = 0u;
-    if (tid < kGroupRows) {  // member tid's entries inside [c0, c0 + chunk): its list ascends
-      int lo = 0, hi = 0;
-      if ((members >> tid) & 1u) {
-        const int row = slot * kGroupRows + tid;
-        const int n = min(p.topk, p.row_len[row]);
-        const int32_t *sel = p.topk_idx + static_cast<size_t>(row) * p.topk;
-        int a = 0, b = n;  // first entry >= c0 (or -1 padding)
-        while (a < b) {
-          const int mid = (a + b) >> 1;
-          const int t = sel[mid];
-          if (t >= 0 && t < c0) a = mid + 1; else b = mid;
-        }
-        lo = a;
-        b = n;
-        while (a < b) {  // first entry >= c0 + chunk
-          const int mid = (a + b) >> 1;
-          const int t = sel[mid];
-          if (t >= 0 && t < c0 + kUnionChunk) a = mid + 1; else b = mid;
-        }
-        hi = a;
-      }
-      s_rng[tid][0] = lo;
-      s_rng[tid][1] = hi;
-    }
+  for (int c0 = 0; c0 < lmax && members != 0u; c0 += kUnionSpan) {
+    for (int i = tid; i < kUnionSpan / 2; i += kUnionThreads) mask2[i] = 0u;
     __syncthreads();
-    // every member's entries at once (entry e of member j at j * span + e),
-    // so the loads of all members are in flight together
-    int span = 0;
-#pragma unroll
-    for (int jj = 0; jj < kGroupRows; ++jj) span = max(span, s_rng[jj][1] - s_rng[jj][0]);
-    for (int f = tid; f < kGroupRows * span; f += kUnionThreads) {
-      const int j = f / span, i = s_rng[j][0] + f % span;
-      if (i >= s_rng[j][1]) continue;  // no member (empty range) or past this member's entries
-      const int row = slot * kGroupRows + j;
-      const int t = p.topk_idx[static_cast<size_t>(row) * p.topk + i];
+    // every member's entries at once (entry i of member j at j * K + i), so
+    // the loads of all members are in flight together
+#pragma unroll 4
+    for (int f = tid; f < kGroupRows * K; f += kUnionThreads) {
+      const int j = f / K, i = f - j * K;
+      if (i >= s_n[j]) continue;  // no member, or past its selected entries
+      const int t = p.topk_idx[static_cast<size_t>(slot * kGroupRows + j) * K + i];
       if (t == -1) continue;
-      if (t < 0 || t >= p.row_len[row]) {
-        flag_status(p.status, DSA_DEV_BAD_INDEX);
+      if (t < 0 || t >= s_len[j]) {
+        if (c0 == 0) flag_status(p.status, DSA_DEV_BAD_INDEX);
         continue;
       }
-      if (t >= c0 && t < c0 + kUnionChunk) atomicOr(&mask2[(t - c0) >> 1], (1u << j) << (16 * ((t - c0) & 1)));
+      if (t >= c0 && t < c0 + kUnionSpan) atomicOr(&mask2[(t - c0) >> 1], (1u << j) << (16 * ((t - c0) & 1)));
     }
     __syncthreads();
-    // thread t: positions c0 + 16t .. +15 (8 threads per 128-position tile);
-    // a selected position on a page outside the pool is flagged and left out
-    constexpr int per = kUnionChunk / kUnionThreads;  // 16
-    int cnt = 0;
-    uint32_t m16[per];  // per position: its 16 row bits
+    for (int s0 = c0; s0 < min(c0 + kUnionSpan, lmax); s0 += kUnionScan) {
+      // thread t: positions s0 + 16t .. +15 (8 threads per 128-position tile);
+      // a selected position on a page outside the pool is flagged and left out
+      constexpr int per = kUnionScan / kUnionThreads;  // 16
+      int cnt = 0;
+      uint32_t m16[per];  // per position: its 16 row bits
 #pragma unroll
-    for (int k = 0; k < per; k += 2) {
-      const int off = tid * per + k;
-      const uint32_t w = mask2[off >> 1];
+      for (int k = 0; k < per; k += 2) {
+        const int off = tid * per + k;
+        const uint32_t w = mask2[(s0 - c0 + off) >> 1];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        m16[k + e] = (w >> (16 * e)) & 0xFFFFu;
-        if (m16[k + e] != 0u) {
-          const int pg = pt[(c0 + off + e) >> p.page_shift];
-          if (pg < 0 || pg >= p.num_pages) {
-            flag_status(p.status, DSA_DEV_BAD_PAGE);
-            m16[k + e] = 0u;
-          } else {
-            ++cnt;
+        for (int e = 0; e < 2; ++e) {
+          m16[k + e] = (w >> (16 * e)) & 0xFFFFu;
+          if (m16[k + e] != 0u) {
+            const int pg = pt[(s0 + off + e) >> p.page_shift];
+            if (pg < 0 || pg >= p.num_pages) {
+              flag_status(p.status, DSA_DEV_BAD_PAGE);
+              m16[k + e] = 0u;
+            } else {
+              ++cnt;
+            }
           }
         }
       }
-    }
-    // stored per tile and row: row j's 128 bits (4 words, bit b of word w =
-    // position 32 w + b of the tile); threads 2i and 2i+1 hold the two
-    // halves of one word, the even one stores rows 0..7, the odd one 8..15
-    {
-      const int ti = (c0 >> 7) + (tid >> 3), wd = (tid >> 1) & 3;
-      const bool odd = (tid & 1) != 0;
+      // stored per tile and row: row j's 128 bits (4 words, bit b of word w =
+      // position 32 w + b of the tile); threads 2i and 2i+1 hold the two
+      // halves of one word, the even one stores rows 0..7, the odd one 8..15
+      {
+        const int ti = (s0 >> 7) + (tid >> 3), wd = (tid >> 1) & 3;
+        const bool odd = (tid & 1) != 0;
 #pragma unroll
-      for (int j = 0; j < kGroupRows; ++j) {
-        uint32_t h = 0u;
+        for (int j = 0; j < kGroupRows; ++j) {
+          uint32_t h = 0u;
 #pragma unroll
-        for (int e = 0; e < per; ++e) h |= ((m16[e] >> j) & 1u) << e;
-        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, h, 1);
-        const uint32_t word = odd ? (other | (h << 16)) : (h | (other << 16));
-        if ((j >= 8) == odd && ti < gp.umax / kGT) msk_out[(static_cast<size_t>(ti) * kGroupRows + j) * 4 + wd] = word;
+          for (int e = 0; e < per; ++e) h |= ((m16[e] >> j) & 1u) << e;
+          const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, h, 1);
+          const uint32_t word = odd ? (other | (h << 16)) : (h | (other << 16));
+          if ((j >= 8) == odd && ti < gp.umax / kGT) msk_out[(static_cast<size_t>(ti) * kGroupRows + j) * 4 + wd] = word;
+        }
       }
-    }
-    // the warp's 4 tiles: lanes 8i .. 8i+7 hold tile i
-    const uint32_t nz = __ballot_sync(0xFFFFFFFFu, cnt > 0);
-    int wcnt = cnt;
+      // the warp's 4 tiles: lanes 8i .. 8i+7 hold tile i
+      const uint32_t nz = __ballot_sync(0xFFFFFFFFu, cnt > 0);
+      int wcnt = cnt;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wcnt += __shfl_xor_sync(0xFFFFFFFFu, wcnt, o);
-    if (lane == 0) {
-      wtiles[warp] = ((nz & 0xFFu) ? 1u : 0u) | ((nz & 0xFF00u) ? 2u : 0u) | ((nz & 0xFF0000u) ? 4u : 0u) |
-                     ((nz & 0xFF000000u) ? 8u : 0u);
-      wsum[warp] = static_cast<uint32_t>(wcnt);
+      for (int o = 16; o > 0; o >>= 1) wcnt += __shfl_xor_sync(0xFFFFFFFFu, wcnt, o);
+      if (lane == 0) {
+        wtiles[warp] = ((nz & 0xFFu) ? 1u : 0u) | ((nz & 0xFF00u) ? 2u : 0u) | ((nz & 0xFF0000u) ? 4u : 0u) |
+                       ((nz & 0xFF000000u) ? 8u : 0u);
+        wsum[warp] = static_cast<uint32_t>(wcnt);
+      }
+      __syncthreads();
+      // the step's tiles with a selected position, in ascending order
+      int before = 0, ctiles = 0, csum = 0;
+      for (int w = 0; w < kUnionThreads / 32; ++w) {
+        const int nt = __popc(wtiles[w]);
+        if (w < warp) before += nt;
+        ctiles += nt;
+        csum += static_cast<int>(wsum[w]);
+      }
+      if (lane < 4 && ((wtiles[warp] >> lane) & 1u)) {
+        const int at = ntile + before + __popc(wtiles[warp] & ((1u << lane) - 1u));
+        const int ti = (s0 >> 7) + warp * 4 + lane;
+        if (at < tmax) tiles_out[at] = ti;
+      }
+      ntile += ctiles;
+      total += csum;
+      __syncthreads();  // every read of mask2, wsum and wtiles is done before the next step
     }
-    __syncthreads();
-    // the chunk's tiles with a selected position, in ascending order
-    int before = 0, ctiles = 0, csum = 0;
-    for (int w = 0; w < kUnionThreads / 32; ++w) {
-      const int nt = __popc(wtiles[w]);
-      if (w < warp) before += nt;
-      ctiles += nt;
-      csum += static_cast<int>(wsum[w]);
-    }
-    if (lane < 4 && ((wtiles[warp] >> lane) & 1u)) {
-      const int at = ntile + before + __popc(wtiles[warp] & ((1u << lane) - 1u));
-      const int ti = (c0 >> 7) + warp * 4 + lane;
-      if (at < tmax) tiles_out[at] = ti;
-    }
-    ntile += ctiles;
-    total += csum;
-    __syncthreads();  // every read of mask2, wsum and wtiles is done before the next chunk
   }
   if (members != 0u && total * 4 < lmax) members = 0u;  // too sparse: the decode kernel does better
   if (tid < kGroupRows && slot * kGroupRows + tid < p.max_rows_attn)
@@ -329,12 +313,6 @@ __device__ __forceinline__ void split2_bf16x2(float x0, float x1, uint32_t &hi, 
   const __nv_bfloat162 r = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
   hi = *reinterpret_cast<const uint32_t *>(&h);
   lo = *reinterpret_cast<const uint32_t *>(&r);
-}
-// One lane of the (fully active) warp: the lowest, so always the same one.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t e;
-  asm volatile("{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.b32 %0, 1, 0, P;\n}\n" : "=r"(e));
-  return e != 0;
 }
 __device__ __forceinline__ bool gwarp_wait(uint32_t bar, uint32_t parity, const volatile int *abort_flag) {
   const bool ok = tc::mbar_wait(bar, parity, abort_flag, kGWaitBudget);
@@ -509,9 +487,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // ================================================================ MMA
     // The whole warp runs the loop with warp-uniform descriptors and one
     // elected lane (always the same one) issues the MMAs and their commits:
-    // a lone issuing thread computes its operands in per-thread registers
-    // and loses most of the tensor rate to the busy softmax warps that share
-    // its scheduler.
+    // a lone issuing thread loses most of the tensor rate to the busy
+    // softmax warps that share its scheduler.
     const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
     const uint32_t idesc_qk = tc::idesc_m128(kGT, false);               // S[q][t]: N = 128 tokens
     const uint32_t idesc_pv = tc::idesc_m128(128, false) | (1u << 16);  // O[q][d]: B (V) MN-major
@@ -525,7 +502,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       return !stop;
     };
     auto commit = [&](uint32_t bar) {
-      if (elect_one()) tc::mma_commit(bar);
+      if (tc::elect_one()) tc::mma_commit(bar);
       __syncwarp();
     };
     // S_w = Q K^T of the next K tile over the 128 head dims (2 swizzle
@@ -535,7 +512,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const int ks = kn % kKStages;
       if (!wait(KFULL(ks), (kn / kKStages) & 1)) return;
       const uint64_t dk = dk0 + ks * kTile;
-      if (elect_one()) {
+      if (tc::elect_one()) {
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -572,7 +549,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const uint64_t dv = dv0 + vs * kTile;
         // O_w += P_w V: the 128 keys as 8 k-steps of 16 (keys 32 c .. +31
         // have their two bf16 terms at columns 32 c and 32 c + 16)
-        if (elect_one()) {
+        if (tc::elect_one()) {
 #pragma unroll
           for (int term = 0; term < 2; ++term)
 #pragma unroll
@@ -804,8 +781,10 @@ int32_t group_union_capacity(const dsa_config_t &cfg) {
 
 cudaError_t launch_group_union(const dsa_config_t &cfg, const AttnParams &p, const GroupParams &gp, cudaStream_t st) {
   (void)cfg;
-  cudaError_t e = launch_pdl(group_union_kernel, dim3(static_cast<unsigned>(gp.nslots)), dim3(kUnionThreads), 0, st,
-                             1u, p, gp);
+  constexpr int smem = kUnionSpan / 2 * 4;
+  cudaError_t e = cudaFuncSetAttribute(group_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(group_union_kernel, dim3(static_cast<unsigned>(gp.nslots)), dim3(kUnionThreads), smem, st, 1u, p, gp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

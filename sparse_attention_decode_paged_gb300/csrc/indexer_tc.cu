@@ -527,35 +527,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ============================================================ MMA
-    if (lane == 0) {
-      // One thread issues everything, so the loop is kept short: the
-      // descriptors' start-address field is linear in the shared-memory
-      // address (every operand lies below 256 KiB), so they are formed once
-      // and advanced by adding offsets >> 4; ring stage, accumulator and
-      // phases are running counters.
-      int cur = -1, qcount = -1, qb = 0;
-      int ms = 0, msphase = 0, ma = 0, maphase = 0;  // ring stage and accumulator of the next tile
-      const uint64_t adesc0 = make_desc<RB>(stage0);
-      const uint32_t batomD = static_cast<uint32_t>(NMAX * RB) >> 4, qpartD = qpartB >> 4;
-      uint64_t ad_s = adesc0, bd_q = 0;
-      uint32_t d = tmem, idesc = 0;
-      bool any = false;
-      // test only: a wait on the MMA-completion barrier before any MMA is
-      // issued, which nothing completes, so it runs out after a short budget
-      const bool test_stop = p.test_timeout != 0 && !tc::mbar_wait(DONE, 0, abort_flag, kTestWaitBudget);
-      for (; wk.valid() && !test_stop; wk.next()) {
-        const int s = ms, ab = ma;
-        if (wk.block != cur) {
-          cur = wk.block;
-          ++qcount;
-          qb = qcount % NQ;
-          idesc = tc::idesc_m128(HP * bc.get(p, cur).nrows, F8);
-          bd_q = make_desc<RB>(q0 + qb * qbufB);
-          if (!tc::mbar_wait(QFULL(qb), (qcount / NQ) & 1, abort_flag, kWaitBudget)) break;
-        }
-        if (!tc::mbar_wait(TEMPTY(ab), maphase ^ 1, abort_flag, kWaitBudget)) break;
-        if (!tc::mbar_wait(FULL(s), msphase, abort_flag, kWaitBudget)) break;
-        tc::tc_fence_after();
+    // The whole warp runs the loop and one elected lane (always the same
+    // one) issues the MMAs and commits, so the descriptors stay
+    // warp-uniform: a lone issuing lane runs far slower beside the busy
+    // epilogue warps on its scheduler.  The descriptors' start-address field
+    // is linear in the shared-memory address (every operand lies below
+    // 256 KiB), so they are formed once and advanced by adding offsets >> 4;
+    // ring stage, accumulator and phases are running counters.
+    const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+    int cur = -1, qcount = -1, qb = 0;
+    int ms = 0, msphase = 0, ma = 0, maphase = 0;  // ring stage and accumulator of the next tile
+    const uint64_t adesc0 = make_desc<RB>(stage0);
+    const uint32_t batomD = static_cast<uint32_t>(NMAX * RB) >> 4, qpartD = qpartB >> 4;
+    uint64_t ad_s = adesc0, bd_q = 0;
+    uint32_t d = tm, idesc = 0;
+    bool any = false, stop = false;
+    auto wait = [&](uint32_t bar, int parity) {
+      if (!warp_wait(bar, static_cast<uint32_t>(parity), abort_flag)) stop = true;
+      return !stop;
+    };
+    // test only: a wait on the MMA-completion barrier before any MMA is
+    // issued, which nothing completes, so it runs out after a short budget
+    const bool test_stop =
+        p.test_timeout != 0 &&
+        !__all_sync(0xFFFFFFFFu, tc::mbar_wait(DONE, 0, abort_flag, kTestWaitBudget));
+    for (; wk.valid() && !test_stop; wk.next()) {
+      const int s = ms, ab = ma;
+      if (wk.block != cur) {
+        cur = wk.block;
+        ++qcount;
+        qb = qcount % NQ;
+        idesc = tc::idesc_m128(HP * bc.get(p, cur).nrows, F8);
+        bd_q = make_desc<RB>(q0 + qb * qbufB);
+        if (!wait(QFULL(qb), (qcount / NQ) & 1)) break;
+      }
+      if (!wait(TEMPTY(ab), maphase ^ 1)) break;
+      if (!wait(FULL(s), msphase)) break;
+      tc::tc_fence_after();
+      if (tc::elect_one()) {
 #pragma unroll
         for (int a = 0; a < ATOMS; ++a)
 #pragma unroll
@@ -570,30 +579,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_commit(EMPTY(s));
         tc::mma_commit(TFULL(ab));
         if (wk.last_of_block()) tc::mma_commit(QEMPTY(qb));
-        any = true;
-        if (++ms == S) {
-          ms = 0;
-          msphase ^= 1;
-          ad_s = adesc0;
-        } else {
-          ad_s += kStageB >> 4;
-        }
-        if (++ma == NACC) {
-          ma = 0;
-          maphase ^= 1;
-          d = tmem;
-        } else {
-          d += static_cast<uint32_t>(NMAX);
-        }
       }
-      if (wk.valid()) {
-        *abort_flag = 1;
-        flag_status(p.status, DSA_DEV_TIMEOUT);
+      __syncwarp();
+      any = true;
+      if (++ms == S) {
+        ms = 0;
+        msphase ^= 1;
+        ad_s = adesc0;
+      } else {
+        ad_s += kStageB >> 4;
       }
-      if (any) {  // every MMA issued here has completed before TMEM is freed
-        tc::mma_commit(DONE);
-        tc::mbar_wait(DONE, 0, nullptr, kWaitBudget);
+      if (++ma == NACC) {
+        ma = 0;
+        maphase ^= 1;
+        d = tm;
+      } else {
+        d += static_cast<uint32_t>(NMAX);
       }
+    }
+    if (wk.valid() && lane == 0) {
+      *abort_flag = 1;
+      flag_status(p.status, DSA_DEV_TIMEOUT);
+    }
+    if (any) {  // every MMA issued here has completed before TMEM is freed
+      if (tc::elect_one()) tc::mma_commit(DONE);
+      __syncwarp();
+      if (lane == 0) tc::mbar_wait(DONE, 0, nullptr, kWaitBudget);
     }
     __syncwarp();
   } else {
@@ -669,12 +680,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 1; i < 4; ++i)
           if (rr == i) L = bi.lens[i];
-        if (t < L) {
-          const float score = sum * sc;
-          // kept in L2 for the top-k that reads them next (the key stream is evict-first)
+        const float score = sum * sc;
+        if (t < L)  // kept in L2 for the top-k that reads them next (the key stream is evict-first)
           tc::st_global_hint(p.scores + static_cast<size_t>(bi.first + rr - p.row_lo) * p.score_width + t, score, keep);
-          if (p.row_hist != nullptr)  // first-level histogram for the top-k that follows
+        if (p.row_hist != nullptr) {
+          // first-level histogram for the top-k that follows.  In a one-row
+          // block the lanes with the same bin add their count with one
+          // atomic (measured: the histogram costs the B64 indexer 2 us
+          // instead of 6, the long-fp8 one 6 instead of 12); multi-row
+          // blocks add key by key, which measured far cheaper there (the
+          // mixed step's indexer: +5 us, against +51 with the matching)
+          const bool live = t < L;
+          if (bi.nrows == 1) {
+            const uint32_t bin = live ? (order_key(score) >> 20) : 0xFFFFFFFFu;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
+            if (live && lane == __ffs(static_cast<int>(peers)) - 1)
+              atomicAdd(p.row_hist + static_cast<size_t>(bi.first) * kKeyBins + bin,
+                        static_cast<uint32_t>(__popc(peers)));
+          } else if (live) {
             atomicAdd(p.row_hist + static_cast<size_t>(bi.first + rr) * kKeyBins + (order_key(score) >> 20), 1u);
+          }
         }
       }
       tc::tc_fence_before();

@@ -49,6 +49,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
   }
 }
 
+// One lane of the (fully active) warp: the lowest, so always the same one.
+// An MMA loop run by the whole warp with one elected issuer keeps its
+// operands warp-uniform; a loop run by one lane alone issues far slower
+// when busy warps share its scheduler.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.b32 %0, 1, 0, P;\n}\n" : "=r"(e));
+  return e != 0;
+}
+
 // -------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
