@@ -85,6 +85,8 @@ def parse_args():
                     help="also write a 256 MiB buffer between timed steps (outside the timed events); "
                          "not needed when a step streams far more than L2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill-groups", action="store_true",
+                    help="every row takes the per-row attention (DSA_FLAG_NO_PREFILL_GROUPS)")
     ap.add_argument("--other-workloads", default="3,4",
                     help="workloads also timed after the headline (comma list, '' for none); "
                          "their numbers go to the line's 'workloads' object")
@@ -511,6 +513,8 @@ def run_dsa(args):
     override["flags"] = dsa.DSA_FLAG_TOPK_HISTOGRAM
     if args.kv_layout == "interleaved":  # a token's K and V rows adjacent: one copy per selected token
         override["flags"] |= dsa.DSA_FLAG_KV_INTERLEAVED
+    if args.no_prefill_groups:
+        override["flags"] |= dsa.DSA_FLAG_NO_PREFILL_GROUPS
     if args.score_buffer_bytes:
         override["score_buffer_bytes"] = args.score_buffer_bytes
     dev = DeviceStep(inp, **override)

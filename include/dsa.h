@@ -146,7 +146,11 @@ enum {
    * launch returns and the scores are incomplete.  The next call without the
    * bit runs normally once the status word is reset.  Never set it outside a
    * test. */
-  DSA_FLAG_TEST_WAIT_TIMEOUT = 1 << 2
+  DSA_FLAG_TEST_WAIT_TIMEOUT = 1 << 2,
+  /* Every row takes the per-row sparse attention (top-k slot splits): no
+   * prefill row groups are formed (see dsa_sparse_attn), the workspace has no
+   * group region, and dsa_suggest_num_splits leaves out the group term. */
+  DSA_FLAG_NO_PREFILL_GROUPS = 1 << 3
 };
 
 /* Every pointer one fused step needs (all device pointers). */

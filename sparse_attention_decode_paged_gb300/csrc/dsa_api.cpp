@@ -178,7 +178,7 @@ dsa_status_t dsa_validate_config(const dsa_config_t *c) {
   if (!(c->sm_scale > 0.f) || !std::isfinite(c->sm_scale))
     return fail(DSA_ERR_INVALID_ARG, "sm_scale must be positive and finite");
   if ((c->flags & ~static_cast<int32_t>(DSA_FLAG_TOPK_HISTOGRAM | DSA_FLAG_KV_INTERLEAVED |
-                                        DSA_FLAG_TEST_WAIT_TIMEOUT)) != 0)
+                                        DSA_FLAG_TEST_WAIT_TIMEOUT | DSA_FLAG_NO_PREFILL_GROUPS)) != 0)
     return fail(DSA_ERR_INVALID_ARG, "unknown flags 0x%x", c->flags);
   if (static_cast<long long>(c->max_reqs) * c->max_pages_per_req > 0x7FFFFFFFLL)
     return fail(DSA_ERR_INVALID_ARG, "page table larger than 2^31 entries");

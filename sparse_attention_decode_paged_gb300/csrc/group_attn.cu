@@ -768,8 +768,8 @@ PFN_cuTensorMapEncodeTiled_v12000 group_tensor_map_encoder() {
 }  // namespace
 
 bool group_path_enabled(const dsa_config_t &cfg) {
-  return cfg.block_rows > 1 && cfg.num_kv_heads * 8 == cfg.num_q_heads && cfg.head_dim == 128 &&
-         cfg.max_rows >= kGroupRows;
+  return (cfg.flags & DSA_FLAG_NO_PREFILL_GROUPS) == 0 && cfg.block_rows > 1 &&
+         cfg.num_kv_heads * 8 == cfg.num_q_heads && cfg.head_dim == 128 && cfg.max_rows >= kGroupRows;
 }
 
 int32_t group_union_capacity(const dsa_config_t &cfg) {

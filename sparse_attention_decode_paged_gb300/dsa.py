@@ -38,6 +38,7 @@ DSA_KEY_FP8_E4M3 = 1
 DSA_FLAG_TOPK_HISTOGRAM = 1 << 0
 DSA_FLAG_KV_INTERLEAVED = 1 << 1
 DSA_FLAG_TEST_WAIT_TIMEOUT = 1 << 2  # test only: one indexer wait runs out (see dsa.h)
+DSA_FLAG_NO_PREFILL_GROUPS = 1 << 3  # every row takes the per-row attention
 
 EXPORTED = (
     "dsa_validate_config", "dsa_workspace_size", "dsa_workspace_layout",

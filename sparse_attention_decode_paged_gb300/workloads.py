@@ -5,7 +5,7 @@ no row building, no scoring, no selection and no attention.  It is shared by
 the CUDA path's tests and benchmark and by the CPU oracle's tests, so both
 sides see identical inputs.
 
-Five workloads, numbered by their seed:
+Seven workloads, numbered by their seed:
 
   0  tiny decode   B=2, lengths {37, 200}, page 16, indexer 4x32, top-k 16,
                    4 q heads / 1 KV head, head dim 64
@@ -25,6 +25,10 @@ Five workloads, numbered by their seed:
                    1 KV head, head dim 128 (the score-window case of a
                    prefill chunk at 1M context, with one KV head so the
                    caches stay a few GB)
+  6  correlated    workload 3's shape and request mix, with the
+                   indexer queries of each 16-row slot [16i, 16i+16) drawn
+                   around one shared base vector (q_idx = base_i + 0.25 e_r),
+                   so consecutive prefill tokens select overlapping keys
 
 The problem statement these follow is Megatron-LM PR #7211 (DSA over GQA
 with paged KV caches): every query token is a row that routes to the top-k
@@ -111,6 +115,10 @@ WORKLOADS = [
         idx_heads=64, idx_dim=128, page_size=64, topk=2048, num_splits=4,
         max_rows=80, max_reqs=3, max_pages_per_req=16384, score_width=1 << 20,
         block_rows=4, idx_key_dtype=KEY_BF16, kind="mixed"),
+    _wl("mixed_correlated_48dec_512prefill", 6, num_q_heads=64, num_kv_heads=8,
+        head_dim=128, idx_heads=64, idx_dim=128, page_size=64, topk=2048,
+        num_splits=4, max_rows=1024, max_reqs=49, max_pages_per_req=512,
+        score_width=32768, block_rows=4, idx_key_dtype=KEY_BF16, kind="mixed"),
 ]
 
 
@@ -228,7 +236,7 @@ def request_mix(wl: Workload):
     elif wl.seed == 2:
         cache_len = np.full(wl.max_reqs, 32768, dtype=np.int32)
         new = np.ones(wl.max_reqs, dtype=np.int32)
-    elif wl.seed == 3:
+    elif wl.seed in (3, 6):
         dec = rng.integers(1024, 32768, size=48, endpoint=True).astype(np.int32)
         cache_len = np.concatenate([dec, np.array([8192 + 512], dtype=np.int32)])
         new = np.concatenate([np.ones(48, dtype=np.int32), np.array([512], dtype=np.int32)])
@@ -287,7 +295,11 @@ def generate(wl: Workload | int, *, with_kv: bool = True):
     P = wl.page_size
     out = dict(workload=wl, cache_len=cache_len, new_tokens=new,
                page_table=pt, num_pages=npool)
-    out["q_idx"] = round_to_bf16_bits(_normal_f32(s, "q_idx", R * HI * DI)).reshape(R, HI, DI)
+    qi = _normal_f32(s, "q_idx", R * HI * DI).reshape(R, HI, DI)
+    if s == 6:  # each 16-row slot's queries around one shared base vector
+        base = _normal_f32(s, "extra", (R + 15) // 16 * HI * DI).reshape(-1, HI, DI)
+        qi = np.repeat(base, 16, axis=0)[:R] + np.float32(0.25) * qi
+    out["q_idx"] = round_to_bf16_bits(qi).reshape(R, HI, DI)
     if s == 0:
         out["w"] = _uniform_f32(s, "w", R * HI).reshape(R, HI)
     else:

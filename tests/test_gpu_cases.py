@@ -472,15 +472,16 @@ def _group_slots(row_req, row_len, idx, wl):
     return groups
 
 
-@pytest.mark.parametrize("splits", [1, 3])
-def test_prefill_groups_vs_oracle(splits, dsa_lib, cuda_ok):
+@pytest.mark.parametrize("i,splits", [(3, 1), (3, 3), (6, 4)])
+def test_prefill_groups_vs_oracle(i, splits, dsa_lib, cuda_ok):
     """The mixed step's prefill rows go through the group kernel: their
     outputs match the oracle on their own selections, and each split's
     partial state matches the oracle over the row's selected positions in
-    that split's union tiles; the decode rows keep the slot splits."""
+    that split's union tiles; the decode rows keep the slot splits.  Workload
+    6 is the same step with correlated indexer queries."""
     from sparse_attention_decode_paged_gb300.harness import DeviceStep
 
-    inp = W.generate(3)
+    inp = W.generate(i)
     wl = inp["workload"]
     dev = DeviceStep(inp, num_splits=splits, flags=dsa_lib.DSA_FLAG_KV_INTERLEAVED)
     dev.step()
@@ -528,3 +529,44 @@ def test_prefill_groups_vs_oracle(splits, dsa_lib, cuda_ok):
         k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel)
         o, _ = O.attention_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads)
         np.testing.assert_allclose(out[r], o, atol=1e-2, rtol=2e-2, err_msg=f"row {r}")
+
+
+def test_no_prefill_groups_flag_takes_the_row_path(dsa_lib, cuda_ok):
+    """With DSA_FLAG_NO_PREFILL_GROUPS the mixed step has no group region and
+    every prefill row takes the per-row attention: outputs and top-k slot
+    split partials match the oracle, and the selection is the grouped
+    step's."""
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    inp = W.generate(3)
+    wl = inp["workload"]
+    flags = dsa_lib.DSA_FLAG_KV_INTERLEAVED
+    dev = DeviceStep(inp, flags=flags | dsa_lib.DSA_FLAG_NO_PREFILL_GROUPS)
+    lay = dsa_lib.dsa_workspace_layout(dev.cfg)
+    assert lay["group"] == lay["key_hist"]
+    dev.step()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    ref = DeviceStep(inp, flags=flags)
+    ref.step()
+    torch.cuda.synchronize()
+    idx = dev.views["topk_idx"].cpu().numpy()
+    assert np.array_equal(idx, ref.views["topk_idx"].cpu().numpy())
+    rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+    out = dev.t["out"].float().cpu().numpy().astype(np.float64)
+    pm = dev.views["part_m"].cpu().numpy().astype(np.float64)
+    pl = dev.views["part_l"].cpu().numpy().astype(np.float64)
+    pa = dev.views["part_acc"].cpu().numpy().astype(np.float64)
+    q = O.bf16_bits_to_f64(inp["q"])
+    for r in list(range(48, 560, 37)) + [559]:  # prefill rows
+        sel = idx[r][idx[r] >= 0]
+        k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel)
+        o, _ = O.attention_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads)
+        np.testing.assert_allclose(out[r], o, atol=1e-2, rtol=2e-2, err_msg=f"row {r}")
+        m, l, acc = O.split_partials_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads, wl.num_splits)
+        fin = np.isfinite(m)
+        assert np.array_equal(fin, np.isfinite(pm[r])), r
+        np.testing.assert_allclose(pm[r][fin], m[fin], atol=1e-2, rtol=2e-2, err_msg=f"m {r}")
+        np.testing.assert_allclose(pl[r][fin], l[fin], rtol=2e-2, atol=0, err_msg=f"l {r}")
+        np.testing.assert_allclose(pa[r][fin] / pl[r][fin][:, None], acc[fin] / l[fin][:, None],
+                                   atol=1e-2, rtol=2e-2, err_msg=f"acc/l {r}")

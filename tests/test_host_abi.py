@@ -58,7 +58,7 @@ def test_validate_config_accepts_all_workloads(dsa_lib):
     (dict(topk=0), 1), (dict(topk=40000), 1), (dict(score_width=40000), 1),
     (dict(num_splits=0), 2), (dict(block_rows=5), 2), (dict(idx_key_dtype=7), 1),
     (dict(sm_scale=-1.0), 1), (dict(sm_scale=float("inf")), 1), (dict(max_rows=0), 1),
-    (dict(flags=8), 1),
+    (dict(flags=16), 1),
 ])
 def test_validate_config_rejects(dsa_lib, bad, status):
     cfg = _cfg(dsa_lib, **bad)
@@ -211,7 +211,7 @@ def test_suggest_num_splits_rule(rows, topk, sms, want, dsa_lib):
 def test_suggest_num_splits_matches_the_workloads(dsa_lib):
     """The parity workloads use the suggestion for a 152-SM GB300 (the tiny
     case keeps 2 splits so the merge runs on it)."""
-    for i in range(1, 5):
+    for i in (1, 2, 3, 4, 6):
         wl = W.workload(i)
         assert dsa_lib.dsa_suggest_num_splits(dsa_lib.config_from_workload(wl, 1000), 152) == wl.num_splits
 
@@ -255,3 +255,17 @@ def test_arena_views_are_aligned_disjoint_and_shaped():
     again = {n: buf[v.data_ptr() - buf.data_ptr():][:v.numel() * v.element_size()] for n, v in views.items()}
     assert torch.equal(again["row_len"].view(torch.int32), torch.tensor([7, 8, 9], dtype=torch.int32))
     assert bool((again["q"].view(torch.bfloat16) == 1.5).all())
+
+
+def test_no_prefill_groups_flag_drops_the_group_region(dsa_lib):
+    """DSA_FLAG_NO_PREFILL_GROUPS: no group region in the workspace and no
+    group term in the split suggestion."""
+    wl = W.workload(3)
+    cfg = dsa_lib.config_from_workload(wl, 1000)
+    lay = dsa_lib.dsa_workspace_layout(cfg)
+    assert lay["key_hist"] > lay["group"]
+    cfg2 = dsa_lib.config_from_workload(wl, 1000, flags=dsa_lib.DSA_FLAG_NO_PREFILL_GROUPS)
+    lay2 = dsa_lib.dsa_workspace_layout(cfg2)
+    assert lay2["group"] == lay2["key_hist"] and lay2["total"] < lay["total"]
+    assert dsa_lib.dsa_suggest_num_splits(cfg, 152) == 4
+    assert dsa_lib.dsa_suggest_num_splits(cfg2, 152) == 1
