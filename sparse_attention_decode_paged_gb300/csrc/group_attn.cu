@@ -23,36 +23,35 @@
 // prefix (else every row stays with the decode kernel, which then moves fewer
 // bytes); its rows are marked so the decode kernel leaves them to this one.
 //
-// group_attn_kernel (persistent, one CTA per SM, 10 warps) walks (slot, KV
+// group_attn_kernel (persistent, one CTA per SM, 11 warps) walks (slot, KV
 // head g, split s) items; split s takes the group's listed tiles
 // [s*T/S, (s+1)*T/S) of its T tiles.  The 128 queries of an item are the
 // slot's 16 rows x 8 query heads of g (query q = 8 * row + head), the MMA's
 // M = 128; a tile's 128 positions are the MMA's N (and the K of P V):
-//  * warp 0 (producer): stages the queries with TMA tile loads, then streams
-//    each listed tile's whole pages of K and V rows of head g with TMA tile
-//    loads (one box per page and 64-element atom, 128-byte swizzle) plus the
-//    tile's row masks into a 2-stage ring; a prefill group's union covers
-//    most of its prefix, so whole pages move with a handful of copies per
-//    tile where a gather of the selected rows alone would need one copy per
-//    few rows;
-//  * warp 1 (MMA, one thread): S = Q K^T (both K-major) into tensor memory,
-//    and O += P V with P read from tensor memory as the A operand and the
-//    page-major V tile read as an MN-major B operand; S of the next tile is
-//    issued before P V of this one;
-//  * warps 2..9 (softmax, two warpgroups each taking one half of every
-//    tile's keys, thread = query) run one pass with a running maximum: the
-//    halves agree on the tile's row maximum over the row's selected keys,
-//    the running maximum m moves only when a tile's exceeds it by more than
-//    2^8 (then l and this row's O are scaled by 2^(m_old - m)), p =
-//    exp2(x - m) <= 256 (fp32) for the selected keys (0 for the rest) is
-//    summed into l and written as two bf16 terms hi + lo into tensor
-//    memory (their sum is p to about 2^-17 relative), and the MMA runs P V
-//    once per term, so the probabilities are not rounded to bf16 before the
-//    value reduction;
-//  * after the item, the softmax threads read O and write the split's
-//    partial state (m, l, acc) of their member row and head.
+//  * warp 0 (K producer): stages the item's queries with TMA tile loads,
+//    then each listed tile's whole pages of K rows of head g (one box per
+//    page and 64-element atom, 128-byte swizzle) plus the tile's row masks
+//    into a 3-stage ring; warp 10 (V producer) streams the same tiles' V
+//    rows into a 2-stage ring.  A prefill group's union covers most of its
+//    prefix, so whole pages move with a handful of copies per tile where a
+//    gather of the selected rows alone would need one copy per few rows;
+//  * warp 1 (MMA; one elected lane issues): S = Q K^T (both K-major) into
+//    tensor memory, and O += P V with P read from tensor memory as the A
+//    operand and the page-major V tile read as an MN-major B operand;
+//  * warps 2..9 (softmax): warpgroup w takes the item's tiles t = w, w + 2,
+//    ... with its own S_w (P_w is written over it) and O_w in tensor memory,
+//    thread = query.  A running maximum m moves only when a tile's row
+//    maximum over the row's selected keys exceeds it by more than 2^8 (then
+//    l and the row's O_w are scaled by 2^(m_old - m)); p = exp2(x - m) <= 256
+//    (fp32) for the selected keys (0 for the rest) is summed into l and
+//    written as two bf16 terms hi + lo (their sum is p to about 2^-17
+//    relative), and the MMA runs P V once per term, so the probabilities are
+//    not rounded to bf16 before the value reduction;
+//  * after the item the two warpgroups combine their row states (exact
+//    maximum, l and O scaled to it) and write the split's partial state
+//    (m, l, acc) of their member rows, warpgroup w head dims [64w, 64w+64).
 // Every wait is bounded; a wait that runs out sets DSA_DEV_TIMEOUT and an
-// abort flag, the producer waits for its copies in flight and the MMA warp
+// abort flag, the producers wait for their copies in flight and the MMA warp
 // for its MMAs before tensor memory is freed.
 #include <cudaTypedefs.h>
 
@@ -69,12 +68,12 @@ constexpr int kGT = 128;                          // union positions per tile (M
 constexpr int kQ = kGroupRows * 8;                // queries per item (MMA M)
 constexpr int kKStages = 3;                       // K tile (and row mask) ring
 constexpr int kVStages = 2;                       // V tile ring
-constexpr int kGWarps = 10;                       // producer, MMA, 2 softmax warpgroups
+constexpr int kGWarps = 11;                       // K producer, MMA, 2 softmax warpgroups, V producer
 constexpr int kGThreads = kGWarps * 32;
 constexpr long long kGWaitBudget = 2000000000LL;  // SM cycles (about 1 s)
-constexpr int kUnionThreads = 512;
+constexpr int kUnionThreads = 1024;
 constexpr int kUnionSpan = 32768;                 // positions per pass (bitmasks in shared memory)
-constexpr int kUnionScan = 8192;                  // positions per scan step (16 per thread)
+constexpr int kUnionScan = 16 * kUnionThreads;    // positions per scan step (16 per thread)
 constexpr float kLn2G = 0.69314718055994530942f;
 
 // tensor-memory columns, per softmax warpgroup w: S_w [128 x 128] fp32 at
@@ -158,7 +157,7 @@ __global__ void __launch_bounds__(kUnionThreads) group_union_kernel(const AttnPa
     __syncthreads();
     // every member's entries at once (entry i of member j at j * K + i), so
     // the loads of all members are in flight together
-#pragma unroll 4
+#pragma unroll 8
     for (int f = tid; f < kGroupRows * K; f += kUnionThreads) {
       const int j = f / K, i = f - j * K;
       if (i >= s_n[j]) continue;  // no member, or past its selected entries
@@ -174,25 +173,25 @@ __global__ void __launch_bounds__(kUnionThreads) group_union_kernel(const AttnPa
     for (int s0 = c0; s0 < min(c0 + kUnionSpan, lmax); s0 += kUnionScan) {
       // thread t: positions s0 + 16t .. +15 (8 threads per 128-position tile);
       // a selected position on a page outside the pool is flagged and left out
-      constexpr int per = kUnionScan / kUnionThreads;  // 16
+      constexpr int per = kUnionScan / kUnionThreads;  // 16, all on one page (page_size >= 16)
       int cnt = 0;
       uint32_t m16[per];  // per position: its 16 row bits
+      uint32_t any = 0u;
 #pragma unroll
       for (int k = 0; k < per; k += 2) {
-        const int off = tid * per + k;
-        const uint32_t w = mask2[(s0 - c0 + off) >> 1];
+        const uint32_t w = mask2[(s0 - c0 + tid * per + k) >> 1];
+        m16[k] = w & 0xFFFFu;
+        m16[k + 1] = w >> 16;
+        any |= w;
+      }
+      if (any != 0u) {
+        const int pg = pt[(s0 + tid * per) >> p.page_shift];
+        const bool bad = pg < 0 || pg >= p.num_pages;
+        if (bad) flag_status(p.status, DSA_DEV_BAD_PAGE);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          m16[k + e] = (w >> (16 * e)) & 0xFFFFu;
-          if (m16[k + e] != 0u) {
-            const int pg = pt[(s0 + off + e) >> p.page_shift];
-            if (pg < 0 || pg >= p.num_pages) {
-              flag_status(p.status, DSA_DEV_BAD_PAGE);
-              m16[k + e] = 0u;
-            } else {
-              ++cnt;
-            }
-          }
+        for (int k = 0; k < per; ++k) {
+          if (bad) m16[k] = 0u;
+          cnt += m16[k] != 0u ? 1 : 0;
         }
       }
       // stored per tile and row: row j's 128 bits (4 words, bit b of word w =
@@ -270,14 +269,13 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a_tmem, uint64_t
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
-// 32 lanes x 32 columns of 32-bit values loaded, the wait in the same block.
-__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 32 lanes x 32 columns loaded without waiting: tmem_wait_ld32 on the same
+// registers must come before any use of them.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
       "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
         "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
@@ -285,8 +283,30 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, float (&v)[32]) {
         "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Waits for this thread's tensor-memory loads; the registers pass through
+// the statement so no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                 "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                 "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+// An empty statement that the registers pass through (orders their uses
+// after the wait that precedes it).
+__device__ __forceinline__ void tmem_fence_regs32(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                 "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                 "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
 }
 // 32 lanes x 16 columns of 32-bit values stored from registers.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -400,8 +420,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   pdl_wait();  // the union and the selection come from the kernels before
 
-  if (warp == 0) {
-    // ============================================================ producer
+  if (warp == 0 || warp == kGWarps - 1) {
+    // ========================================================== producers
+    // warp 0 stages each item's queries, then its tiles' K rows and row
+    // masks into the K ring; the last warp stages the tiles' V rows into
+    // the V ring.  Apart, each runs as far ahead as its own ring allows, so
+    // the K stream (and the next item's queries) never waits behind V.
+    const bool vrole = warp == kGWarps - 1;
     const uint64_t policy = tc::l2_evict_first_policy();
     const uint64_t qpolicy = tc::l2_evict_last_policy();
     int kn = 0, vn = 0, qn = 0;  // K tiles, V tiles and query sets issued
@@ -426,16 +451,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
                                                                  gp.grouped[x.slot * kGroupRows + lane] != 0))) - 1;
         pt += static_cast<size_t>(p.row_req[row0 < 0 ? 0 : row0]) * p.max_pages_per_req;
       }
-      // queries: rows (16 slot rows x 8 heads of g) of the [R * Hq, D] view
-      if (!wait(QEMPTY, (qn & 1) ^ 1)) break;
-      if (lane == 0) tc::mbar_arrive_expect_tx(QFULL, kQ * 256u);
-      __syncwarp();
-      if (lane < 2 * kGroupRows) {
-        const int j = lane >> 1, a = lane & 1;
-        tc::tma_load_2d(q0 + a * (kQ * 128u) + j * 1024u, &qmap, a * 64,
-                        (x.slot * kGroupRows + j) * Hq + x.g * 8, QFULL, qpolicy);
+      if (!vrole) {
+        // queries: rows (16 slot rows x 8 heads of g) of the [R * Hq, D] view
+        if (!wait(QEMPTY, (qn & 1) ^ 1)) break;
+        if (lane == 0) tc::mbar_arrive_expect_tx(QFULL, kQ * 256u);
+        __syncwarp();
+        if (lane < 2 * kGroupRows) {
+          const int j = lane >> 1, a = lane & 1;
+          tc::tma_load_2d(q0 + a * (kQ * 128u) + j * 1024u, &qmap, a * 64,
+                          (x.slot * kGroupRows + j) * Hq + x.g * 8, QFULL, qpolicy);
+        }
+        ++qn;
       }
-      ++qn;
       const int32_t *tiles = gp.tiles + static_cast<size_t>(x.slot) * (gp.umax / kGT);
       const uint32_t *umask = gp.umask + static_cast<size_t>(x.slot) * (gp.umax / kGT) * 64;
       const int P = p.page_size, npg = kGT / P;  // pages per tile: 1, 2, 4 or 8
@@ -450,28 +477,29 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const int pg = pi < p.max_pages_per_req ? pt[pi] : -1;
           if (pg >= 0 && pg < p.num_pages) rowc = pg * P;
         }
-        // K rows and the tile's row masks
-        const int ks = kn % kKStages;
-        if (!wait(KEMPTY(ks), ((kn / kKStages) & 1) ^ 1)) break;
-        if (lane == 0) {
-          tc::mbar_arrive_expect_tx(KFULL(ks), kGT * 256u + kGT * 2u);
-          tc::bulk_load(base + lay.off_mask + ks * kGT * 2u, umask + static_cast<size_t>(ti) * 64, kGT * 2u, KFULL(ks),
-                        qpolicy);
+        if (!vrole) {  // K rows and the tile's row masks
+          const int ks = kn % kKStages;
+          if (!wait(KEMPTY(ks), ((kn / kKStages) & 1) ^ 1)) break;
+          if (lane == 0) {
+            tc::mbar_arrive_expect_tx(KFULL(ks), kGT * 256u + kGT * 2u);
+            tc::bulk_load(base + lay.off_mask + ks * kGT * 2u, umask + static_cast<size_t>(ti) * 64, kGT * 2u,
+                          KFULL(ks), qpolicy);
+          }
+          __syncwarp();
+          if (lane < 2 * npg)
+            tc::tma_load_2d(base + lay.off_k + ks * (kGT * 256u) + a * (kGT * 128u) + k * P * 128u, &kmap,
+                            kcol0 + x.g * 128 + a * 64, rowc, KFULL(ks), policy);
+          ++kn;
+        } else {  // V rows
+          const int vs = vn % kVStages;
+          if (!wait(VEMPTY(vs), ((vn / kVStages) & 1) ^ 1)) break;
+          if (lane == 0) tc::mbar_arrive_expect_tx(VFULL(vs), kGT * 256u);
+          __syncwarp();
+          if (lane < 2 * npg)
+            tc::tma_load_2d(base + lay.off_v + vs * (kGT * 256u) + a * (kGT * 128u) + k * P * 128u, &vmap,
+                            vcol0 + x.g * 128 + a * 64, rowc, VFULL(vs), policy);
+          ++vn;
         }
-        __syncwarp();
-        if (lane < 2 * npg)
-          tc::tma_load_2d(base + lay.off_k + ks * (kGT * 256u) + a * (kGT * 128u) + k * P * 128u, &kmap,
-                          kcol0 + x.g * 128 + a * 64, rowc, KFULL(ks), policy);
-        ++kn;
-        // V rows
-        const int vs = vn % kVStages;
-        if (!wait(VEMPTY(vs), ((vn / kVStages) & 1) ^ 1)) break;
-        if (lane == 0) tc::mbar_arrive_expect_tx(VFULL(vs), kGT * 256u);
-        __syncwarp();
-        if (lane < 2 * npg)
-          tc::tma_load_2d(base + lay.off_v + vs * (kGT * 256u) + a * (kGT * 128u) + k * P * 128u, &vmap,
-                          vcol0 + x.g * 128 + a * 64, rowc, VFULL(vs), policy);
-        ++vn;
       }
     }
     // no copy may land after the CTA exits
@@ -632,16 +660,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const uint4 sel = *reinterpret_cast<const uint4 *>(masks_s + ks * 64 + j * 4);
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(KEMPTY(ks));  // the masks are in registers
-        float mt = -INFINITY;  // unscaled score maximum over them
+        // the unscaled score maximum over them: two loads in flight at a
+        // time, eight independent max chains
+        float mx[8];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float v[32];
-          tmem_ld32_sync(colS + 32 * ch, v);
-          const uint32_t sw = ch == 0 ? sel.x : ch == 1 ? sel.y : ch == 2 ? sel.z : sel.w;
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ch += 2) {
+          uint32_t sa[32], sb[32];
+          tmem_ld32_nowait(colS + 32 * ch, sa);
+          tmem_ld32_nowait(colS + 32 * ch + 32, sb);
+          tmem_wait_ld32(sa);
+          tmem_fence_regs32(sb);
+          const uint32_t wa = ch == 0 ? sel.x : sel.z, wb = ch == 0 ? sel.y : sel.w;
 #pragma unroll
-          for (int kk = 0; kk < 32; ++kk)
-            if ((sw >> kk) & 1u) mt = fmaxf(mt, v[kk]);
+          for (int kk = 0; kk < 32; ++kk) {
+            if ((wa >> kk) & 1u) mx[kk & 7] = fmaxf(mx[kk & 7], __uint_as_float(sa[kk]));
+            if ((wb >> kk) & 1u) mx[kk & 7] = fmaxf(mx[kk & 7], __uint_as_float(sb[kk]));
+          }
         }
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float mn = mt * c;  // c > 0: the tile's row maximum of the scaled (log2-domain) scores
         mtrue = fmaxf(mtrue, mn);
         float alpha = 1.f;
@@ -666,25 +705,28 @@ __global__ void __launch_bounds__(kGThreads, 1)
           }
         }
         const float mb = m == -INFINITY ? 0.f : -m;  // no selected key yet: every p is 0
+        // keys 32 ch .. +31: P_w's two terms go to S_w's columns of these
+        // keys (read just before), hi to 32 ch .. +15 and lo to 32 ch + 16 ..
+        float la[4] = {0.f, 0.f, 0.f, 0.f};  // independent sum chains
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
-          // keys 32 ch .. +31: P_w's two terms go to S_w's columns of these
-          // keys (read just before), hi to 32 ch .. +15 and lo to 32 ch + 16 ..
-          float v[32];
-          tmem_ld32_sync(colS + 32 * ch, v);
+          uint32_t v[32];
+          tmem_ld32_nowait(colS + 32 * ch, v);
+          tmem_wait_ld32(v);
           const uint32_t sw = ch == 0 ? sel.x : ch == 1 ? sel.y : ch == 2 ? sel.z : sel.w;
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float x0 = ((sw >> (2 * k)) & 1u) ? v[2 * k] : -INFINITY;
-            const float x1 = ((sw >> (2 * k + 1)) & 1u) ? v[2 * k + 1] : -INFINITY;
+            const float x0 = ((sw >> (2 * k)) & 1u) ? __uint_as_float(v[2 * k]) : -INFINITY;
+            const float x1 = ((sw >> (2 * k + 1)) & 1u) ? __uint_as_float(v[2 * k + 1]) : -INFINITY;
             const float p0 = ex2_approx(fmaf(x0, c, mb)), p1 = ex2_approx(fmaf(x1, c, mb));
-            l += p0 + p1;
+            la[k & 3] += p0 + p1;
             split2_bf16x2(p0, p1, hi[k], lo[k]);
           }
           tmem_st16(colS + 32 * ch, hi);
           tmem_st16(colS + 32 * ch + 16, lo);
         }
+        l += (la[0] + la[1]) + (la[2] + la[3]);
         tmem_st_wait();
         tc::tc_fence_before();
         __syncwarp();
