@@ -171,11 +171,29 @@ inline int merge_pairs_per_warp(int S) { return S <= 3 ? 8 : S <= 6 ? 4 : S <= 1
 
 template <int D, int PPW>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
-  pdl_wait();  // the partials come from the attention kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long total = static_cast<long long>(p.max_rows) * p.num_q_heads;
   const long long rh0 = (static_cast<long long>(blockIdx.x) * 8 + warp) * PPW;  // first (row, head)
+  // rows of length 0 (pad rows) hold only empty partials: their outputs are
+  // written as such without reading them (row lengths are step inputs, read
+  // before the wait for the attention kernel)
+  bool empty = false;
+  if (p.row_len != nullptr && rh0 < total) {
+    const long long last = std::min(rh0 + PPW, total) - 1;
+    empty = true;
+    for (long long r = rh0 / p.num_q_heads; r <= last / p.num_q_heads; ++r) empty = empty && p.row_len[r] == 0;
+  }
+  pdl_wait();  // the partials come from the attention kernel
   if (rh0 >= total) return;
+  if (empty) {
+    for (long long rh = rh0; rh < std::min(rh0 + PPW, total); ++rh) {
+      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + rh * D;
+      for (int d = lane * 2; d < D; d += 64)
+        *reinterpret_cast<__nv_bfloat162 *>(dst + d) = __floats2bfloat162_rn(0.f, 0.f);
+      if (p.lse && lane == 0) p.lse[rh] = -INFINITY;
+    }
+    return;
+  }
   if constexpr (PPW == 1)
     merge_one<D>(p.part_m, p.part_l, p.part_acc, rh0, p.num_splits, p.out, p.lse, lane);
   else

@@ -397,6 +397,29 @@ dsa_status_t topk_impl(const dsa_config_t *cfg, int32_t row_begin, int32_t row_e
 }
 }  // namespace
 
+namespace {
+dsa_status_t merge_impl(const dsa_config_t *cfg, const float *part_m, const float *part_l, const float *part_acc,
+                        void *out, float *lse, const int32_t *row_len, dsa_stream_t stream) {
+  DSA_CHECK_CFG(cfg);
+  DSA_CHECK_DEV_PTR(part_m);
+  DSA_CHECK_DEV_PTR(part_l);
+  DSA_CHECK_DEV_PTR(part_acc);
+  DSA_CHECK_DEV_PTR(out);
+  if (lse != nullptr && !aligned16(lse)) return fail(DSA_ERR_INVALID_ARG, "lse is not 16-byte aligned");
+  dsa::MergeParams p;
+  p.part_m = part_m;
+  p.part_l = part_l;
+  p.part_acc = part_acc;
+  p.out = static_cast<uint8_t *>(out);
+  p.lse = lse;
+  p.row_len = row_len;
+  p.max_rows = cfg->max_rows;
+  p.num_q_heads = cfg->num_q_heads;
+  p.num_splits = cfg->num_splits;
+  return cuda_status(dsa::launch_merge(*cfg, p, stream), "merge launch");
+}
+}  // namespace
+
 extern "C" {
 
 dsa_status_t dsa_indexer_scores(const dsa_config_t *cfg, const void *q_idx, const float *w,
@@ -496,24 +519,10 @@ dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void 
   return cuda_status(dsa::launch_sparse_attn(*cfg, p, stream), "sparse attention launch");
 }
 
+
 dsa_status_t dsa_merge(const dsa_config_t *cfg, const float *part_m, const float *part_l,
                        const float *part_acc, void *out, float *lse, dsa_stream_t stream) {
-  DSA_CHECK_CFG(cfg);
-  DSA_CHECK_DEV_PTR(part_m);
-  DSA_CHECK_DEV_PTR(part_l);
-  DSA_CHECK_DEV_PTR(part_acc);
-  DSA_CHECK_DEV_PTR(out);
-  if (lse != nullptr && !aligned16(lse)) return fail(DSA_ERR_INVALID_ARG, "lse is not 16-byte aligned");
-  dsa::MergeParams p;
-  p.part_m = part_m;
-  p.part_l = part_l;
-  p.part_acc = part_acc;
-  p.out = static_cast<uint8_t *>(out);
-  p.lse = lse;
-  p.max_rows = cfg->max_rows;
-  p.num_q_heads = cfg->num_q_heads;
-  p.num_splits = cfg->num_splits;
-  return cuda_status(dsa::launch_merge(*cfg, p, stream), "merge launch");
+  return merge_impl(cfg, part_m, part_l, part_acc, out, lse, nullptr, stream);
 }
 
 dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *a, void *workspace,
@@ -546,7 +555,8 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *a, void *w
   st = dsa_sparse_attn(cfg, a->q, a->k_cache, a->v_cache, a->page_table, a->row_req, a->row_len,
                        topk_idx, part_m, part_l, part_acc, workspace, stream);
   if (st != DSA_OK) return st;
-  return dsa_merge(cfg, part_m, part_l, part_acc, a->out, a->lse, stream);
+  // the step knows its rows: pad rows are written empty without their partials
+  return merge_impl(cfg, part_m, part_l, part_acc, a->out, a->lse, a->row_len, stream);
 }
 
 const char *dsa_last_error(void) { return g_last_error.c_str(); }

@@ -76,6 +76,7 @@ struct MergeParams {
   const float *part_m, *part_l, *part_acc;
   uint8_t *out;  // bf16 [R, Hq, D]
   float *lse;    // [R, Hq] or null
+  const int32_t *row_len;  // [R] or null: a row of length 0 is written empty without reading its partials
   int32_t max_rows, num_q_heads, num_splits;
 };
 
