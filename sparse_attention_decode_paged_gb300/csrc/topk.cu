@@ -480,15 +480,23 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
 // result is the same, bit for bit.
 // ---------------------------------------------------------------------------
 constexpr int kStreamCluster = 8;
+constexpr int kMaxStreamWidth = 1 << 22;                  // the longest row (score_width) supported
 constexpr int kStreamU = 4;                               // float4 loads per lane and step
 constexpr int kStreamStep = 4 * 32 * kStreamU;            // keys per warp step
 constexpr int kStreamSegAlign = kStreamStep * kWarps;     // a CTA segment is a multiple of this
+
+constexpr int kSelMax = 4096;                             // top-k sizes the one-pass path takes
+constexpr int kStreamWordsMax = (kMaxStreamWidth / kStreamCluster) / 32;  // a segment's bitmap words
 
 struct StreamShared {
   uint32_t hist[kBins1];        // this CTA's counts (read by the whole cluster)
   uint32_t hist_tot[kBins1];    // the row's counts
   uint32_t cand[kCandMax];      // this CTA's candidates (read by the whole cluster)
   uint32_t all_cand[kCandMax];  // the cluster's candidates
+  uint32_t cand_pos[kCandMax];  // one-pass path: the positions of this CTA's candidates
+  uint32_t sel_pos[kSelMax];    // one-pass path: positions of this CTA's keys above the threshold bin
+  uint32_t bits[kStreamWordsMax];  // one-pass path: one bit per position of this CTA's segment
+  uint32_t nsel, cta_n, tie_cut;
   uint32_t scan[kWarps];
   uint32_t wgt[kWarps], weq[kWarps];  // per warp: keys > tau and == tau in its range, then their prefixes
   uint32_t count;                     // this CTA's candidates
@@ -512,6 +520,25 @@ __device__ __forceinline__ void load_keys4(const float *srow, int i, int end, bo
 #pragma unroll
     for (int j = 0; j < 4; ++j) k[j] = j < nv ? order_key(__ldcg(srow + i + j)) : 0u;
   }
+}
+
+// The block's set bits of sh.bits[0, nwords) in ascending order: returns
+// each thread's first rank (exclusive prefix of the counts of the threads
+// before it; thread t holds words [t*per, (t+1)*per)) and the block's total.
+__device__ __forceinline__ uint32_t bits_prefix(StreamShared &sh, int nwords, int per, uint32_t &total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t cnt = 0u;
+  for (int w = tid * per; w < min(nwords, (tid + 1) * per); ++w) cnt += __popc(sh.bits[w]);
+  const uint32_t incl = warp_incl_scan(cnt, lane);
+  if (lane == 31) sh.scan[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t v = warp_incl_scan(sh.scan[lane], lane);
+    sh.scan[lane] = v;
+  }
+  __syncthreads();
+  total = sh.scan[kWarps - 1];
+  return incl - cnt + (warp > 0 ? sh.scan[warp - 1] : 0u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_stream_kernel(const TopkParams p) {
@@ -599,6 +626,158 @@ __global__ void __launch_bounds__(kThreads, 1) topk_stream_kernel(const TopkPara
   need -= sh.above;
   const uint32_t in_bin = sh.hist_tot[d1];
   uint32_t prefix = d1 << 20, mask = 0xFFF00000u;
+
+  if (in_bin <= static_cast<uint32_t>(kCandMax) && K <= kSelMax) {
+    // ---- one pass over the row: a key above the threshold bin is selected
+    // (its position kept), a key inside it is a candidate (key and position
+    // kept); everything after this runs on chip
+    if (tid == 0) {
+      sh.count = 0u;
+      sh.nsel = 0u;
+    }
+    __syncthreads();
+    for (int base = wlo; base < whi; base += kStreamStep) {
+      uint32_t k[kStreamU][4];
+      int nv[kStreamU];
+#pragma unroll
+      for (int u = 0; u < kStreamU; ++u) load_keys4(srow, base + u * 128 + 4 * lane, whi, vec, k[u], nv[u]);
+#pragma unroll
+      for (int u = 0; u < kStreamU; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nv[u]) {
+            const uint32_t kb = k[u][j] & mask;
+            const uint32_t pos = static_cast<uint32_t>(base + u * 128 + 4 * lane + j);
+            if (kb > prefix) {
+              const uint32_t at = atomicAdd(&sh.nsel, 1u);
+              if (at < static_cast<uint32_t>(kSelMax)) sh.sel_pos[at] = pos;
+            } else if (kb == prefix) {
+              const uint32_t at = atomicAdd(&sh.count, 1u);
+              if (at < static_cast<uint32_t>(kCandMax)) {
+                sh.cand[at] = k[u][j];
+                sh.cand_pos[at] = pos;
+              }
+            }
+          }
+    }
+    __syncthreads();
+    cl.sync();  // every CTA's candidates are complete (and the row histogram was read)
+    if (ghist != nullptr && q == 0)
+      for (int i = tid; i < kBins1; i += kThreads) ghist[i] = 0u;  // ready for the next step
+    uint32_t total = 0u;
+    for (int rr = 0; rr < C; ++rr) {
+      const uint32_t cnt = min(*cl.map_shared_rank(&sh.count, rr), static_cast<uint32_t>(kCandMax));
+      const uint32_t *src = cl.map_shared_rank(sh.cand, rr);
+      for (uint32_t i = tid; i < cnt && total + i < static_cast<uint32_t>(kCandMax); i += kThreads)
+        sh.all_cand[total + i] = src[i];
+      total += cnt;
+    }
+    if (tid == 0 && q == 0) {
+      if (total > static_cast<uint32_t>(kCandMax)) flag_status(p.status, DSA_DEV_BAD_ROW);  // scores vs histogram
+      if (total != in_bin) flag_status(p.status, DSA_DEV_BAD_HIST);
+    }
+    total = min(total, static_cast<uint32_t>(kCandMax));
+    __syncthreads();
+#pragma unroll 1
+    for (int shift = 10; shift >= 0; shift -= 10) {
+      const uint32_t dg = radix_pass(sh, sh.all_cand, total, shift, prefix, mask, need);
+      prefix |= dg << shift;
+      mask |= 0x3FFu << shift;
+    }
+    const uint32_t tau = prefix;  // `need` keys equal to tau still fit
+    // this CTA's candidates above tau (all selected) and equal to it
+    const uint32_t own = min(sh.count, static_cast<uint32_t>(kCandMax));
+    uint32_t gt = 0u, eq = 0u;
+    for (uint32_t i = tid; i < own; i += kThreads) {
+      gt += sh.cand[i] > tau ? 1u : 0u;
+      eq += sh.cand[i] == tau ? 1u : 0u;
+    }
+    gt = warp_sum(gt);
+    eq = warp_sum(eq);
+    if (lane == 0) {
+      sh.wgt[warp] = gt;
+      sh.weq[warp] = eq;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t tg = 0u, te = 0u;
+      for (int w = 0; w < kWarps; ++w) {
+        tg += sh.wgt[w];
+        te += sh.weq[w];
+      }
+      sh.cta_gt = tg;
+      sh.cta_eq = te;
+    }
+    __syncthreads();
+    cl.sync();  // every CTA's tie count is visible
+    // ties are taken in position order: the CTAs before this one come first
+    uint32_t e_before = 0u;
+    for (int rr = 0; rr < q; ++rr) e_before += *cl.map_shared_rank(&sh.cta_eq, rr);
+    const uint32_t eq_cta = sh.cta_eq;
+    const uint32_t allowed = need > e_before ? min(need - e_before, eq_cta) : 0u;
+    const int nwords = (hi - lo + 31) / 32;
+    const int per = (nwords + kThreads - 1) / kThreads;
+    // the position of this CTA's allowed-th tie (when only some of them fit)
+    if (tid == 0) sh.tie_cut = allowed == eq_cta ? 0xFFFFFFFFu : 0u;
+    if (allowed > 0u && allowed < eq_cta) {
+      for (int w = tid; w < nwords; w += kThreads) sh.bits[w] = 0u;
+      __syncthreads();
+      for (uint32_t i = tid; i < own; i += kThreads)
+        if (sh.cand[i] == tau) {
+          const uint32_t b = sh.cand_pos[i] - static_cast<uint32_t>(lo);
+          atomicOr(&sh.bits[b >> 5], 1u << (b & 31));
+        }
+      __syncthreads();
+      uint32_t tot;
+      uint32_t rank = bits_prefix(sh, nwords, per, tot);
+      for (int w = tid * per; w < min(nwords, (tid + 1) * per); ++w) {
+        uint32_t bw = sh.bits[w];
+        while (bw != 0u) {
+          const int b = __ffs(static_cast<int>(bw)) - 1;
+          if (rank == allowed - 1u) sh.tie_cut = static_cast<uint32_t>(lo + w * 32 + b);
+          ++rank;
+          bw &= bw - 1u;
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t tie_cut = sh.tie_cut;
+    // this CTA's selection, marked in its segment's bitmap
+    for (int w = tid; w < nwords; w += kThreads) sh.bits[w] = 0u;
+    __syncthreads();
+    const uint32_t nsel = min(sh.nsel, static_cast<uint32_t>(kSelMax));
+    for (uint32_t i = tid; i < nsel; i += kThreads) {
+      const uint32_t b = sh.sel_pos[i] - static_cast<uint32_t>(lo);
+      atomicOr(&sh.bits[b >> 5], 1u << (b & 31));
+    }
+    for (uint32_t i = tid; i < own; i += kThreads) {
+      const uint32_t key = sh.cand[i], pos = sh.cand_pos[i];
+      if (key > tau || (key == tau && allowed > 0u && pos <= tie_cut)) {
+        const uint32_t b = pos - static_cast<uint32_t>(lo);
+        atomicOr(&sh.bits[b >> 5], 1u << (b & 31));
+      }
+    }
+    if (tid == 0) sh.cta_n = nsel + sh.cta_gt + allowed;
+    __syncthreads();
+    cl.sync();  // every CTA's count is visible
+    uint32_t offset = 0u;
+    for (int rr = 0; rr < q; ++rr) offset += *cl.map_shared_rank(&sh.cta_n, rr);
+    uint32_t tot;
+    uint32_t rank = offset + bits_prefix(sh, nwords, per, tot);
+    for (int w = tid * per; w < min(nwords, (tid + 1) * per); ++w) {
+      uint32_t bw = sh.bits[w];
+      while (bw != 0u) {
+        const int b = __ffs(static_cast<int>(bw)) - 1;
+        if (rank < static_cast<uint32_t>(K)) out[rank] = lo + w * 32 + b;
+        ++rank;
+        bw &= bw - 1u;
+      }
+    }
+    if (tid == 0 && q == C - 1 && offset + tot != static_cast<uint32_t>(K))
+      flag_status(p.status, DSA_DEV_BAD_HIST);  // the counts do not add up to k
+    cl.sync();  // keep this CTA's shared memory alive until the cluster is done with it
+    return;
+  }
 
   // ---- C. the threshold key tau and how many keys equal to it still fit
   if (in_bin <= static_cast<uint32_t>(kCandMax)) {

@@ -72,11 +72,14 @@ def _topk_cfg(dsa_lib, R, W_, K):
 
 # widths reach each cluster size of the in-shared-memory top-k: 1 CTA (300,
 # 4096), 2 (32768), 4 (65536, 131072) and 8 (262144, the longest row it
-# holds); past that the streaming top-k reads the score buffer in every
-# pass: 262148 and 1M / 4M keys (float4 loads), 262147 (a row stride that is
-# not a multiple of 4: scalar loads)
+# holds); past that the streaming top-k reads the score buffer: 262148 and
+# 1M / 4M keys (float4 loads), 262147 (a row stride that is not a multiple
+# of 4: scalar loads).  It reads a row once when k <= 4096 and the
+# threshold bin holds at most 4096 keys (the all-ties rows do not), else in
+# several passes (also k = 5000)
 @pytest.mark.parametrize("W_,K", [(4096, 512), (32768, 2048), (65536, 1024), (131072, 2048), (262144, 2048),
-                                  (300, 16), (262147, 300), (262148, 512), (1 << 20, 2048), (1 << 22, 2048)])
+                                  (300, 16), (262147, 300), (262148, 512), (262148, 5000), (1 << 20, 2048),
+                                  (1 << 22, 2048)])
 def test_topk_crafted_rows(W_, K, dsa_lib, cuda_ok):
     rng = np.random.default_rng(W_ + K)
     R = 12
@@ -280,7 +283,7 @@ def test_device_bounds_flags(dsa_lib, cuda_ok):
 # ----------------------------------------------------------------------------
 # indexer -> top-k histogram hand-off (DSA_FLAG_TOPK_HISTOGRAM, always on in dsa_step)
 # ----------------------------------------------------------------------------
-@pytest.mark.parametrize("i", [1, 3, 4])
+@pytest.mark.parametrize("i", [1, 3, 4, 5])  # 5: 1M-key rows, the streaming top-k
 def test_topk_histogram_handoff(i, dsa_lib, cuda_ok):
     from sparse_attention_decode_paged_gb300.harness import DeviceStep
 
