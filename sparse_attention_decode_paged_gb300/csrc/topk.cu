@@ -464,9 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
 // indexer's exact first-level histogram names the k-th key's bin before any
 // score is read, so a pass keeps only that bin's keys on chip).
 //
-// One cluster of kStreamCluster CTAs per row; CTA q owns a contiguous
-// segment of the row and warp w of the CTA a contiguous range of that
-// segment, read in steps of kStreamU float4 loads per lane:
+// One cluster of 2, 4 or 8 CTAs per row; CTA q owns a contiguous segment of
+// the row (at most 512K keys) and warp w of the CTA a contiguous range of
+// that segment, read in steps of kStreamU float4 loads per lane:
 //  A. the row's histogram: the indexer's counts if they total the row
 //     length, else counted in one pass and summed over the cluster;
 //  B. the bin of the k-th key; C. one pass copies out the keys inside it
@@ -486,7 +486,8 @@ constexpr int kStreamStep = 4 * 32 * kStreamU;            // keys per warp step
 constexpr int kStreamSegAlign = kStreamStep * kWarps;     // a CTA segment is a multiple of this
 
 constexpr int kSelMax = 4096;                             // top-k sizes the one-pass path takes
-constexpr int kStreamWordsMax = (kMaxStreamWidth / kStreamCluster) / 32;  // a segment's bitmap words
+constexpr int kStreamSegMax = kMaxStreamWidth / kStreamCluster;  // the longest CTA segment (512K keys)
+constexpr int kStreamWordsMax = kStreamSegMax / 32;               // its bitmap words
 
 struct StreamShared {
   uint32_t hist[kBins1];        // this CTA's counts (read by the whole cluster)
@@ -970,8 +971,21 @@ cudaError_t launch_topk(const dsa_config_t &cfg, const TopkParams &p, int rows, 
     cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = launch_pdl(topk_stream_kernel, dim3(static_cast<unsigned>(rows * kStreamCluster)), dim3(kThreads), smem,
-                   st, static_cast<unsigned>(kStreamCluster), p);
+    // CTAs per row: at least what keeps a CTA's segment within its bitmap
+    // (512K keys), more (up to 8) while the rows' clusters still fit on the
+    // GPU at once; an 8-CTA cluster needs 8 free SMs of one GPC, and only
+    // 15 of them fit at a time (1M prefill: 66 rows, 195 us with 8 CTAs per
+    // row)
+    int sms = 0, dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int c_min = (cfg.score_width + kStreamSegMax - 1) / kStreamSegMax;
+    int c = 2;
+    while (c < kStreamCluster && static_cast<long long>(rows) * c * 2 <= sms) c *= 2;
+    c = std::max(c, c_min);
+    c = c <= 2 ? 2 : c <= 4 ? 4 : 8;
+    e = launch_pdl(topk_stream_kernel, dim3(static_cast<unsigned>(rows * c)), dim3(kThreads), smem, st,
+                   static_cast<unsigned>(c), p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
