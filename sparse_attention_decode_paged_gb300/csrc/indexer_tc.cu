@@ -635,14 +635,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if ((it & 1) != wg) continue;  // the other warpgroup's tile
-      if (!warp_wait(TFULL(ab), aphase, abort_flag)) {
-        if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
-        break;
-      }
-      tc::tc_fence_after();
       const int t = wk.tile() * kTok + tl;
       float sc = 1.f;
       if constexpr (F8) {
+        // the key's scale (two dependent loads: page id, then scale) is
+        // fetched before the wait for the accumulator, so its latency
+        // overlaps the tile's MMA instead of following it
         sc = 0.f;
         if (t < bi.lmax) {
           const int pg = pt[t / p.page_size];
@@ -650,6 +648,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             sc = p.idx_scale[static_cast<size_t>(pg) * p.page_size + t % p.page_size];
         }
       }
+      if (!warp_wait(TFULL(ab), aphase, abort_flag)) {
+        if (lane == 0) { *abort_flag = 1; flag_status(p.status, DSA_DEV_TIMEOUT); }
+        break;
+      }
+      tc::tc_fence_after();
       const float *wq = wbuf + qb * NMAX;
       const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(ab * NMAX);
       for (int rr = 0; rr < bi.nrows; ++rr) {
