@@ -886,17 +886,40 @@ def run_e2e(args, dsa, dev, inp, stream, flush):
         with torch.cuda.graph(graph, stream=stream):
             device_part(torch.cuda.current_stream())
         stream.synchronize()
-        times, eager = [], []
+        times, eager, host_t, dev_t = [], [], [], []
+        ge = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         for k in range(args.e2e_steps + 3):
             if args.flush:
                 flush.fill_(k & 0xFF)
             stream.synchronize()
             t0 = time.perf_counter()
             host_rows()
+            t1 = time.perf_counter()
+            ge[0].record(stream)
             graph.replay()
+            ge[1].record(stream)
             stream.synchronize()
             if k >= 3:
                 times.append(time.perf_counter() - t0)
+                host_t.append(t1 - t0)
+                dev_t.append(ge[0].elapsed_time(ge[1]) * 1e-3)
+        # where the device time goes: the same three operations issued
+        # eagerly with events between them
+        pe = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        parts = {"h2d": [], "step": [], "d2h": []}
+        for k in range(min(args.e2e_steps, 20) + 3):
+            stream.synchronize()
+            pe[0].record(stream)
+            dev.inputs.copy_(h_in, non_blocking=True)
+            pe[1].record(stream)
+            dsa.dsa_step(cfg, dev.args, dev.workspace, stream)
+            pe[2].record(stream)
+            h_out.copy_(dev.outputs, non_blocking=True)
+            pe[3].record(stream)
+            stream.synchronize()
+            if k >= 3:
+                for i, n in enumerate(("h2d", "step", "d2h")):
+                    parts[n].append(pe[i].elapsed_time(pe[i + 1]) * 1e3)
         for k in range(args.e2e_steps + 3):
             if args.flush:
                 flush.fill_(k & 0xFF)
@@ -907,9 +930,18 @@ def run_e2e(args, dsa, dev, inp, stream, flush):
             stream.synchronize()
             if k >= 3:
                 eager.append(time.perf_counter() - t0)
-    return {"value": statistics.median(times) * 1e6, "unit": "us", "h2d_bytes_per_step": int(h2d),
+    wall, host_us, dev_us = statistics.median(times) * 1e6, statistics.median(host_t) * 1e6, statistics.median(dev_t) * 1e6
+    return {"value": wall, "unit": "us", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": len(times),
             "eager_us": statistics.median(eager) * 1e6,
+            "split_us": {"host_rows": host_us, "graph_on_device": dev_us,
+                         "launch_and_wait": wall - host_us - dev_us,
+                         "h2d_eager": statistics.median(parts["h2d"]), "step_eager": statistics.median(parts["step"]),
+                         "d2h_eager": statistics.median(parts["d2h"]),
+                         "note": "medians: host_rows = dsa_build_rows into pinned staging (host clock); "
+                                 "graph_on_device = CUDA events around the graph replay (H2D + step + D2H); "
+                                 "launch_and_wait = the rest of the wall time (graph launch, host wait); the "
+                                 "*_eager parts time the three operations one by one"},
             "path": "dsa_build_rows into the pinned input staging + one CUDA-graph replay of (one H2D copy of "
                     "the input arena, dsa_step, one D2H copy of the output arena) + host wait, wall clock "
                     "median; eager_us: the same calls issued eagerly"}
