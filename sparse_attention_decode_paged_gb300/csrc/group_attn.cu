@@ -269,33 +269,6 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a_tmem, uint64_t
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
-// 32 lanes x 32 columns loaded without waiting: tmem_wait_ld32 on the same
-// registers must come before any use of them.
-__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
-      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
-// Waits for this thread's tensor-memory loads; the registers pass through
-// the statement so no use of them is scheduled before it.
-__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
-                 "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
-                 "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-               :
-               : "memory");
-}
 // An empty statement that the registers pass through (orders their uses
 // after the wait that precedes it).
 __device__ __forceinline__ void tmem_fence_regs32(uint32_t (&r)[32]) {
@@ -668,9 +641,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll 1
         for (int ch = 0; ch < 4; ch += 2) {
           uint32_t sa[32], sb[32];
-          tmem_ld32_nowait(colS + 32 * ch, sa);
-          tmem_ld32_nowait(colS + 32 * ch + 32, sb);
-          tmem_wait_ld32(sa);
+          tc::tmem_ld32_nowait(colS + 32 * ch, sa);
+          tc::tmem_ld32_nowait(colS + 32 * ch + 32, sb);
+          tc::tmem_wait_ld32(sa);
           tmem_fence_regs32(sb);
           const uint32_t wa = ch == 0 ? sel.x : sel.z, wb = ch == 0 ? sel.y : sel.w;
 #pragma unroll
@@ -711,8 +684,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t v[32];
-          tmem_ld32_nowait(colS + 32 * ch, v);
-          tmem_wait_ld32(v);
+          tc::tmem_ld32_nowait(colS + 32 * ch, v);
+          tc::tmem_wait_ld32(v);
           const uint32_t sw = ch == 0 ? sel.x : ch == 1 ? sel.y : ch == 2 ? sel.z : sel.w;
           uint32_t hi[16], lo[16];
 #pragma unroll

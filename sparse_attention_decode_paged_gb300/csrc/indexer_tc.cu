@@ -655,35 +655,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tc_fence_after();
       const float *wq = wbuf + qb * NMAX;
       const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(ab * NMAX);
-      for (int rr = 0; rr < bi.nrows; ++rr) {
-        float sum = 0.f;
-        if (HP == 64) {
-          float v[64];
-          tc::tmem_ld64_sync(trow + rr * 64, v);
-          const float4 *w4 = reinterpret_cast<const float4 *>(wq + rr * 64);
+      // every row's weighted sum first, so the accumulator goes back to the
+      // MMA before the stores and histogram atomics; with 64 heads the
+      // accumulator is read in 32-column chunks, the next chunk's load in
+      // flight while one is summed
+      float sums[4] = {0.f, 0.f, 0.f, 0.f};
+      if (HP == 64 && bi.nrows == 1) {  // one row: one load of its 64 heads
+        float v[64];
+        tc::tmem_ld64_sync(trow, v);
+        const float4 *w4 = reinterpret_cast<const float4 *>(wq);
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 ww = w4[i];
+          s4[0] = fmaf(ww.x, fmaxf(v[4 * i], 0.f), s4[0]);
+          s4[1] = fmaf(ww.y, fmaxf(v[4 * i + 1], 0.f), s4[1]);
+          s4[2] = fmaf(ww.z, fmaxf(v[4 * i + 2], 0.f), s4[2]);
+          s4[3] = fmaf(ww.w, fmaxf(v[4 * i + 3], 0.f), s4[3]);
+        }
+        sums[0] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      } else if (HP == 64) {
+        const int nch = 2 * bi.nrows;
+        uint32_t ca[32], cb[32];
+        auto add = [&](const uint32_t (&v)[32], int c) {
+          const float4 *w4 = reinterpret_cast<const float4 *>(wq + c * 32);
           float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < 8; ++i) {
             const float4 ww = w4[i];
-            s4[0] = fmaf(ww.x, fmaxf(v[4 * i], 0.f), s4[0]);
-            s4[1] = fmaf(ww.y, fmaxf(v[4 * i + 1], 0.f), s4[1]);
-            s4[2] = fmaf(ww.z, fmaxf(v[4 * i + 2], 0.f), s4[2]);
-            s4[3] = fmaf(ww.w, fmaxf(v[4 * i + 3], 0.f), s4[3]);
+            s4[0] = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * i]), 0.f), s4[0]);
+            s4[1] = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s4[1]);
+            s4[2] = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s4[2]);
+            s4[3] = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s4[3]);
           }
-          sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-        } else {
+          const float part = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            if (r == (c >> 1)) sums[r] += part;
+        };
+        tc::tmem_ld32_nowait(trow, ca);
+#pragma unroll
+        for (int c = 0; c < 8; c += 2) {
+          if (c < nch) {
+            tc::tmem_wait_ld32(ca);
+            if (c + 1 < nch) tc::tmem_ld32_nowait(trow + (c + 1) * 32, cb);
+            add(ca, c);
+          }
+          if (c + 1 < nch) {
+            tc::tmem_wait_ld32(cb);
+            if (c + 2 < nch) tc::tmem_ld32_nowait(trow + (c + 2) * 32, ca);
+            add(cb, c + 1);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          if (rr >= bi.nrows) break;
+          float sum = 0.f;
           for (int c = 0; c < HP; c += 16) {
             float v[16];
             tc::tmem_ld16_sync(trow + rr * HP + c, v);
 #pragma unroll
             for (int i = 0; i < 16; ++i) sum = fmaf(wq[rr * HP + c + i], fmaxf(v[i], 0.f), sum);
           }
+          sums[rr] = sum;
         }
-        int L = bi.lens[0];
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(TEMPTY(ab));  // the accumulator is read
 #pragma unroll
-        for (int i = 1; i < 4; ++i)
-          if (rr == i) L = bi.lens[i];
-        const float score = sum * sc;
+      for (int rr = 0; rr < 4; ++rr) {
+        if (rr >= bi.nrows) break;
+        const int L = bi.lens[rr];
+        const float score = sums[rr] * sc;
         if (t < L)  // kept in L2 for the top-k that reads them next (the key stream is evict-first)
           tc::st_global_hint(p.scores + static_cast<size_t>(bi.first + rr - p.row_lo) * p.score_width + t, score, keep);
         if (p.row_hist != nullptr) {
@@ -705,9 +750,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(TEMPTY(ab));
     }
   }
 
