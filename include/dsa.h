@@ -412,7 +412,7 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *args, void
  * this entry point; it exists for those callers.
  *
  * The step's intermediates (status word, scores, top-k, split partials,
- * key histogram) go
+ * prefill-group region, key histogram) go
  * to a 32 MiB array inside the library's device image instead of a caller
  * workspace; every GPU that loads the library holds those 32 MiB until the
  * process exits.  Configs whose dsa_workspace_size exceeds 32 MiB are
@@ -442,7 +442,8 @@ const char *dsa_last_error(void);
  * (its size changed; rebuild callers), and the _window calls,
  * dsa_score_windows and dsa_suggest_num_splits were added.  0.3:
  * dsa_workspace_layout_t gained `group` (its size changed), prefill row
- * groups attend on the tensor cores, score_width may reach 4194304. */
+ * groups attend on the tensor cores (DSA_FLAG_NO_PREFILL_GROUPS turns them
+ * off), score_width may reach 4194304. */
 const char *dsa_version(void);
 
 #ifdef __cplusplus

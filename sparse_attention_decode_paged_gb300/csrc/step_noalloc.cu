@@ -5,9 +5,10 @@
 // capturable operation), runtimes whose device memory belongs to another
 // allocator that must not be bypassed or fragmented, and plain C hosts that
 // have no device allocator of their own.  This entry point gives them the
-// step with its intermediates (status word, scores, top-k, split partials)
-// in a fixed-size array that lives in this library's device image.  The
-// caller still passes every input and output.
+// step with its intermediates (status word, scores, top-k, split partials,
+// prefill-group region, key histogram) in a fixed-size array that lives in
+// this library's device image.  The caller still passes every input and
+// output.
 //
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds kNoAllocScratchBytes of it until the process exits.  Its
@@ -20,7 +21,8 @@
 // each row's counts after using them), but the region's offset and size
 // follow the config, so a call whose layout differs from the previous
 // call's on that device first clears its histogram region on `stream`.
-// Scores, top-k and partials are fully rewritten before they are read.
+// Scores, top-k, the prefill-group region and the partials are rewritten
+// before they are read.
 // Calls whose executions overlap on the GPU (different streams, or graphs
 // replayed concurrently) race on the array.
 #include <cuda_runtime.h>
