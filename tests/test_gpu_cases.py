@@ -573,3 +573,32 @@ def test_no_prefill_groups_flag_takes_the_row_path(dsa_lib, cuda_ok):
         np.testing.assert_allclose(pl[r][fin], l[fin], rtol=2e-2, atol=0, err_msg=f"l {r}")
         np.testing.assert_allclose(pa[r][fin] / pl[r][fin][:, None], acc[fin] / l[fin][:, None],
                                    atol=1e-2, rtol=2e-2, err_msg=f"acc/l {r}")
+
+
+@pytest.mark.parametrize("P", [16, 32, 128])
+def test_prefill_groups_other_page_sizes(P, dsa_lib, cuda_ok):
+    """The group kernel moves whole pages per 128-position tile (8, 4 or 1
+    page boxes per tile, or one box per tile for 128-token pages): the mixed
+    step with other page sizes forms the same groups and its group rows'
+    outputs match the oracle."""
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    wl = dataclasses.replace(W.workload(3), page_size=P, max_pages_per_req=32768 // P)
+    inp = W.generate(wl)
+    dev = DeviceStep(inp, flags=dsa_lib.DSA_FLAG_KV_INTERLEAVED)
+    dev.step()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+    idx = dev.views["topk_idx"].cpu().numpy()
+    groups = _group_slots(rows["row_req"], rows["row_len"], idx, wl)
+    assert len(groups) == 32
+    out = dev.t["out"].float().cpu().numpy().astype(np.float64)
+    q = O.bf16_bits_to_f64(inp["q"])
+    for slot in sorted(groups)[::8]:
+        members, _ = groups[slot]
+        for r in (members[0], members[-1]):
+            sel = idx[r][idx[r] >= 0]
+            k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel)
+            o, _ = O.attention_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads)
+            np.testing.assert_allclose(out[r], o, atol=1e-2, rtol=2e-2, err_msg=f"P {P} row {r}")
