@@ -675,11 +675,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         sums[0] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
       } else if (HP == 64) {
+        // the same four chains per row as the one-load path, carried across
+        // the row's two chunks, so a row's score has the same bits whatever
+        // block (or window) it is scored in
         const int nch = 2 * bi.nrows;
         uint32_t ca[32], cb[32];
+        float s4r[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) s4r[r][k] = 0.f;
         auto add = [&](const uint32_t (&v)[32], int c) {
           const float4 *w4 = reinterpret_cast<const float4 *>(wq + c * 32);
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+          float (&s4)[4] = s4r[c >> 1];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float4 ww = w4[i];
@@ -688,10 +696,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             s4[2] = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s4[2]);
             s4[3] = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s4[3]);
           }
-          const float part = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            if (r == (c >> 1)) sums[r] += part;
         };
         tc::tmem_ld32_nowait(trow, ca);
 #pragma unroll
@@ -707,6 +711,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             add(cb, c + 1);
           }
         }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sums[r] = (s4r[r][0] + s4r[r][1]) + (s4r[r][2] + s4r[r][3]);
       } else {
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
