@@ -57,6 +57,7 @@
 
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "dsa_common.cuh"
 #include "tc_ptx.cuh"
@@ -200,11 +201,25 @@ __global__ void __launch_bounds__(kUnionThreads) group_union_kernel(const AttnPa
       {
         const int ti = (s0 >> 7) + (tid >> 3), wd = (tid >> 1) & 3;
         const bool odd = (tid & 1) != 0;
+        // transpose the 16 x 16 bit matrix (m16[e] bit j -> m16[j] bit e)
+        // by swapping 8-, 4-, 2- and 1-wide blocks
+        auto swap_blocks = [&](auto sw_c, uint32_t msk) {
+          constexpr int sw = decltype(sw_c)::value;
+#pragma unroll
+          for (int i = 0; i < per; ++i)
+            if ((i & sw) == 0) {
+              const uint32_t t = ((m16[i] >> sw) ^ m16[i + sw]) & msk;
+              m16[i + sw] ^= t;
+              m16[i] ^= t << sw;
+            }
+        };
+        swap_blocks(std::integral_constant<int, 8>{}, 0x00FFu);
+        swap_blocks(std::integral_constant<int, 4>{}, 0x0F0Fu);
+        swap_blocks(std::integral_constant<int, 2>{}, 0x3333u);
+        swap_blocks(std::integral_constant<int, 1>{}, 0x5555u);
 #pragma unroll
         for (int j = 0; j < kGroupRows; ++j) {
-          uint32_t h = 0u;
-#pragma unroll
-          for (int e = 0; e < per; ++e) h |= ((m16[e] >> j) & 1u) << e;
+          const uint32_t h = m16[j];  // row j's bits of this thread's 16 positions
           const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, h, 1);
           const uint32_t word = odd ? (other | (h << 16)) : (h | (other << 16));
           if ((j >= 8) == odd && ti < gp.umax / kGT) msk_out[(static_cast<size_t>(ti) * kGroupRows + j) * 4 + wd] = word;
