@@ -29,12 +29,21 @@ def _bf16_bits_of(x):
 # ----------------------------------------------------------------------------
 # indexer: integer-valued inputs make every fp32 sum exact
 # ----------------------------------------------------------------------------
-@pytest.mark.parametrize("fp8", [False, True])
-def test_indexer_exact_on_integer_inputs(fp8, dsa_lib, cuda_ok):
-    wl = W.workload(1)
+@pytest.mark.parametrize("fp8,P,br", [(False, 64, 1), (False, 64, 4), (True, 64, 1), (True, 16, 1), (True, 32, 1),
+                                      (True, 128, 1), (True, 64, 2), (True, 64, 4)])
+def test_indexer_exact_on_integer_inputs(fp8, P, br, dsa_lib, cuda_ok):
+    """Exact scores for bf16 and fp8 keys, at every page size (the producer
+    issues one box per page, 1 to 8 per tile) and with score blocks of 1, 2
+    and 4 rows.  With br > 1 the last request appends 9 tokens, so its rows
+    form 2- or 4-row blocks and a shorter last block."""
+    wl = dataclasses.replace(W.workload(1), page_size=P, max_pages_per_req=4096 // P, block_rows=br,
+                             max_rows=16 if br > 1 else 8)
     if fp8:
         wl = dataclasses.replace(wl, idx_key_dtype=W.KEY_FP8_E4M3)
     inp = W.generate(wl)
+    if br > 1:
+        inp["new_tokens"] = inp["new_tokens"].copy()
+        inp["new_tokens"][-1] = 9
     rng = np.random.default_rng(21)
     R, HI, DI = wl.max_rows, wl.idx_heads, wl.idx_dim
     q = rng.integers(-3, 4, (R, HI, DI)).astype(np.float32)
@@ -59,6 +68,25 @@ def test_indexer_exact_on_integer_inputs(fp8, dsa_lib, cuda_ok):
         L = rows["row_len"][r]
         assert np.array_equal(got[r, :L], want[r, :L]), r
     assert dev.status() == 0
+
+    if fp8 and P == 32:
+        # a page id outside the pool inside row 1: flagged, and every key on
+        # the other pages (the same tiles included) still scores exactly
+        r = 1
+        req, j = int(rows["row_req"][r]), 3
+        assert rows["row_len"][r] > (j + 1) * P
+        dev.t["page_table"][req, j] = inp["num_pages"] + 3
+        dev.step()
+        torch.cuda.synchronize()
+        assert dev.status() & dsa_lib.DSA_DEV_BAD_PAGE
+        got = dev.views["scores"].cpu().numpy().astype(np.float64)
+        keep = np.ones(rows["row_len"][r], bool)
+        keep[j * P:(j + 1) * P] = False
+        assert np.array_equal(got[r, :rows["row_len"][r]][keep], want[r, :rows["row_len"][r]][keep])
+        for r2 in range(rows["num_rows"]):
+            if rows["row_req"][r2] != req:
+                L = rows["row_len"][r2]
+                assert np.array_equal(got[r2, :L], want[r2, :L]), r2
 
 
 # ----------------------------------------------------------------------------
