@@ -697,9 +697,20 @@ def run_dsa(args):
         probe = run_read_probe(dev, nbytes["indexer"], stream)
     except Exception as exc:  # a measurement aid; report, do not fail the run
         probe = {"error": repr(exc)[:200]}
+    kv_probe = None
+    if args.kv_layout == "interleaved" and per_row_kv is None:
+        try:
+            kv_probe = run_read_probe_kv(dev, stream)
+        except Exception as exc:
+            kv_probe = {"error": repr(exc)[:200]}
+        probe = dict(probe, kv_rows=kv_probe)
     if "us" in probe:
-        for n in ("indexer", "sparse_attn"):  # same byte count; the attention gathers 2 KiB rows instead
-            kernel_table[n]["frac_of_read_probe"] = (nbytes[n] / (k_ms[n] * 1e-3) / 1e9) / probe["gbs"]
+        kernel_table["indexer"]["frac_of_read_probe"] = (nbytes["indexer"] / (k_ms["indexer"] * 1e-3) / 1e9) / probe["gbs"]
+        # the attention against the same read of its own 4 KiB K/V rows when
+        # measured, else against the page read
+        ref = kv_probe if kv_probe is not None and "gbs" in kv_probe else probe
+        kernel_table["sparse_attn"]["frac_of_read_probe"] = (
+            (nbytes["sparse_attn"] / (k_ms["sparse_attn"] * 1e-3) / 1e9) / ref["gbs"])
 
     others = {}
     wanted = [int(x) for x in args.other_workloads.split(",") if x.strip()] if args.other_workloads else []
@@ -812,6 +823,52 @@ def run_other_workload(i: int, args, stream, peak: float) -> dict:
     del dev, g
     torch.cuda.empty_cache()
     return rec
+
+
+def _probe_reads(base_ptr, order, page_bytes, stream, reps=25):
+    """Median µs of CUDA-event-timed launches of the plain read probe over
+    `order` (device int32 chunk indices) chunks of `page_bytes` from base."""
+    import ctypes
+    import torch
+    from sparse_attention_decode_paged_gb300 import build as B
+    lib = ctypes.CDLL(B.PROBE_LIB)
+    lib.dsa_probe_read_pages.restype = ctypes.c_int
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sink = torch.empty(16 * sms * 256 // 32, dtype=torch.int32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    times = []
+    for _ in range(reps):
+        ev[0].record(stream)
+        rc = lib.dsa_probe_read_pages(ctypes.c_void_p(base_ptr), ctypes.c_void_p(order.data_ptr()), int(order.numel()),
+                                      page_bytes, ctypes.c_void_p(sink.data_ptr()), 16, 256,
+                                      ctypes.c_void_p(stream.cuda_stream))
+        ev[1].record(stream)
+        stream.synchronize()
+        if rc != 0:
+            raise RuntimeError(f"cuda error {rc}")
+        times.append(ev[0].elapsed_time(ev[1]))
+    return statistics.median(times[5:]) * 1e3
+
+
+def run_read_probe_kv(dev, stream):
+    """The same plain read over the K/V rows the step's attention gathers: one
+    4 KiB interleaved K/V row per selected token (the step's own selection),
+    row after row in selection order."""
+    import torch
+    wl = dev.inp["workload"]
+    nr = int(dev.rows["num_rows"])
+    idx = dev.views["topk_idx"][:nr]
+    req = dev.t["row_req"][:nr].long()
+    P = wl.page_size
+    pos = idx.clamp(min=0).long()
+    tok = dev.t["page_table"].long()[req[:, None], pos // P] * P + pos % P
+    order = tok[idx >= 0].to(torch.int32).contiguous()
+    row_bytes = 2 * wl.num_kv_heads * wl.head_dim * 2
+    t_us = _probe_reads(dev.t["k_cache"].data_ptr(), order, row_bytes, stream)
+    nbytes = int(order.numel()) * row_bytes
+    return {"bytes": nbytes, "us": t_us, "gbs": nbytes / (t_us * 1e-6) / 1e9,
+            "what": "plain read of the attention's selected K/V rows (4 KiB each, interleaved cache) in selection "
+                    "order, 16-byte loads, 16x256 threads per SM, median of CUDA-event-timed launches"}
 
 
 def run_read_probe(dev, nbytes_idx, stream, reps=25):
