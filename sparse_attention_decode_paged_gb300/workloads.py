@@ -119,6 +119,13 @@ WORKLOADS = [
         head_dim=128, idx_heads=64, idx_dim=128, page_size=64, topk=2048,
         num_splits=4, max_rows=1024, max_reqs=49, max_pages_per_req=512,
         score_width=32768, block_rows=4, idx_key_dtype=KEY_BF16, kind="mixed"),
+    # the largest row count the library takes: a fresh 4095-token prompt
+    # (row j sees j + 1 keys) and one decode row; 8 query heads per KV head
+    # at head dim 128, so the prompt's 16-row slots form prefill groups
+    _wl("prompt4095_plus_decode_max_rows", 7, num_q_heads=8, num_kv_heads=1,
+        head_dim=128, idx_heads=16, idx_dim=64, page_size=64, topk=256,
+        num_splits=2, max_rows=4096, max_reqs=2, max_pages_per_req=128,
+        score_width=8192, block_rows=4, idx_key_dtype=KEY_BF16, kind="mixed"),
 ]
 
 
@@ -243,6 +250,10 @@ def request_mix(wl: Workload):
     elif wl.seed == 4:
         cache_len = rng.integers(1024, 131072, size=16, endpoint=True).astype(np.int32)
         new = np.ones(16, dtype=np.int32)
+    elif wl.seed == 7:
+        dec = int(rng.integers(4096, 8192, endpoint=True))
+        cache_len = np.array([4095, dec], dtype=np.int32)
+        new = np.array([4095, 1], dtype=np.int32)
     elif wl.seed == 5:
         near = int(rng.integers((1 << 20) - 4096, 1 << 20, endpoint=True))
         short = int(rng.integers(4096, 65536, endpoint=True))

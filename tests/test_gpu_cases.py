@@ -630,3 +630,51 @@ def test_prefill_groups_other_page_sizes(P, dsa_lib, cuda_ok):
             k, v = O.kv_rows(inp, int(rows["row_req"][r]), sel)
             o, _ = O.attention_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads)
             np.testing.assert_allclose(out[r], o, atol=1e-2, rtol=2e-2, err_msg=f"P {P} row {r}")
+
+
+# ----------------------------------------------------------------------------
+# the largest row count
+# ----------------------------------------------------------------------------
+def test_maximum_rows_vs_oracle(dsa_lib, cuda_ok):
+    """4096 rows, the most a config takes: a fresh 4095-token prompt (row j
+    sees j + 1 keys, so rows up to 256 keys select every position) in 4-row
+    score blocks plus one decode row.  The indexer's first CTAs span more
+    short blocks than their block cache holds (the rest are read from global
+    memory), the top-k runs 4096 one-CTA rows, and the prompt's 16-row slots
+    form prefill groups.  Sampled rows' scores, selections and outputs match
+    the oracle; the grouped rows are the ones the stated rule picks."""
+    from sparse_attention_decode_paged_gb300.harness import DeviceStep
+
+    inp = W.generate(7)
+    wl = inp["workload"]
+    dev = DeviceStep(inp, flags=dsa_lib.DSA_FLAG_KV_INTERLEAVED)
+    dev.step()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    rows = O.build_rows(inp["cache_len"], inp["new_tokens"], wl.max_rows, wl.block_rows)
+    assert rows["num_rows"] == 4096
+    scores = dev.views["scores"].cpu().numpy()
+    idx = dev.views["topk_idx"].cpu().numpy()
+    out = dev.t["out"].float().cpu().numpy().astype(np.float64)
+    qi = O.bf16_bits_to_f64(inp["q_idx"])
+    q = O.bf16_bits_to_f64(inp["q"])
+    for r in (0, 1, 2, 3, 4, 127, 255, 256, 257, 1023, 2048, 2049, 3001, 4093, 4094, 4095):
+        L, req = int(rows["row_len"][r]), int(rows["row_req"][r])
+        keys, sc = O.index_keys(inp, req, L)
+        want = O.indexer_scores_row(qi[r], inp["w"][r], keys, sc)
+        tol = 2e-2 * np.abs(want) + 2e-2 * np.sqrt(np.mean(want ** 2))
+        assert (np.abs(scores[r, :L] - want) <= tol).all(), r
+        assert np.array_equal(idx[r], O.topk_row(scores[r], L, wl.topk)), r
+        sel = idx[r][idx[r] >= 0]
+        assert sel.size == min(L, wl.topk), r
+        k, v = O.kv_rows(inp, req, sel)
+        o, _ = O.attention_row(q[r], k, v, wl.sm_scale, wl.num_kv_heads)
+        np.testing.assert_allclose(out[r], o, atol=1e-2, rtol=2e-2, err_msg=f"row {r}")
+    groups = _group_slots(rows["row_req"], rows["row_len"], idx, wl)
+    assert len(groups) > 200
+    lay = dsa_lib.dsa_workspace_layout(dev.cfg)
+    grouped = dev.workspace[lay["group"]:lay["group"] + 4 * wl.max_rows].view(torch.int32).cpu().numpy()
+    want_grouped = np.zeros(wl.max_rows, np.int32)
+    for m, _ in groups.values():
+        want_grouped[m] = 1
+    assert np.array_equal(grouped, want_grouped)
