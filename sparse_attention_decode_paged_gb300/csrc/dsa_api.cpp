@@ -508,13 +508,16 @@ dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void 
   while ((1 << p.page_shift) < cfg->page_size) ++p.page_shift;  // page_size is a validated power of two
   p.grouped = nullptr;
   if (dsa::group_path_enabled(*cfg)) {
-    // prefill row groups: the union, their tensor-core attention, then the
-    // other rows (the decode kernel leaves the grouped rows alone)
+    // prefill row groups: the union, the other rows (the decode kernel leaves
+    // the grouped rows alone), then the groups' tensor-core attention, whose
+    // split partials — most of the step's — are then the last written before
+    // the merge reads them
     const dsa::GroupParams gp = group_params(cfg, workspace);
     p.grouped = gp.grouped;
     cudaError_t e = dsa::launch_group_union(*cfg, p, gp, stream);
+    if (e == cudaSuccess) e = dsa::launch_sparse_attn(*cfg, p, stream);
     if (e == cudaSuccess) e = dsa::launch_group_attn(*cfg, p, gp, stream);
-    if (e != cudaSuccess) return cuda_status(e, "prefill-group attention launch");
+    return cuda_status(e, "prefill-group attention launch");
   }
   return cuda_status(dsa::launch_sparse_attn(*cfg, p, stream), "sparse attention launch");
 }
