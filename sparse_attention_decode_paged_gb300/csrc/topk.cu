@@ -60,7 +60,7 @@ struct TopkShared {
   uint32_t cand[kCandMax];     // this CTA's candidates (read by the whole cluster)
   uint32_t all_cand[kCandMax];  // the cluster's candidates
   uint32_t wtot[kGroupsMax][kWarps];  // per group and warp: (keys > tau) << 16 | (keys == tau)
-  uint32_t gbase[kGroupsMax];         // the same, summed over the CTA's earlier groups and warps
+  uint32_t gbase[kGroupsMax];         // the same, per group: its total over the CTA's warps
   uint32_t scan[kWarps];
   uint32_t count;           // this CTA's candidates
   uint32_t cta_gt, cta_eq;  // this CTA's totals (read by later ranks)
@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
     part = warp_sum(part);
     if (lane == 0) sh.scan[warp] = part;
   }
+  if (tid == 0) sh.count = 0u;  // the candidate count (phase B)
   __syncthreads();  // keys, row histogram, scan
   if (!recount) {
     uint32_t total = 0u;
@@ -288,14 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
         nh += __popc(hits[u]);
       }
     }
-    // offsets from a block scan of the per-thread counts (no shared atomics)
+    // offsets: a warp scan of the per-thread counts and one shared atomic
+    // per warp (the candidates' order is irrelevant: only counts follow)
     const uint32_t incl = warp_incl_scan(nh, lane);
-    if (lane == 31) sh.scan[warp] = incl;
-    __syncthreads();
-    const uint32_t wt = sh.scan[lane];  // warp lane's total
-    const uint32_t wincl = warp_incl_scan(wt, lane);
-    uint32_t base = __shfl_sync(0xFFFFFFFFu, wincl - wt, warp) + incl - nh;
-    if (tid == kThreads - 1) sh.count = base + nh;
+    uint32_t wbase = 0u;
+    if (lane == 31 && incl != 0u) wbase = atomicAdd(&sh.count, incl);
+    uint32_t base = __shfl_sync(0xFFFFFFFFu, wbase, 31) + incl - nh;
 #pragma unroll
     for (int u = 0; u < NG; ++u) {
       if (u < ng && hits[u]) {
@@ -413,27 +412,24 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const TopkPar
     if (lane == 31) sh.gbase[warp] = iv;  // the group's total for now
   }
   __syncthreads();
-  if (tid == 0) {
+  if (tid == 0) {  // this CTA's totals, for the later ranks of the cluster
     uint32_t run = 0u;
-    for (int u = 0; u < ng; ++u) {
-      const uint32_t t = sh.gbase[u];
-      sh.gbase[u] = run;
-      run += t;
-    }
+    for (int u = 0; u < ng; ++u) run += sh.gbase[u];
     sh.cta_gt = run >> 16;
     sh.cta_eq = run & 0xFFFFu;
   }
-  __syncthreads();
-  cl.sync();  // every CTA's totals are visible
+  cl.sync();  // every CTA's totals are visible (and a barrier of this CTA)
   uint32_t g_cta = 0u, e_cta = 0u;
   for (int rr = 0; rr < q; ++rr) {
     g_cta += *cl.map_shared_rank(&sh.cta_gt, rr);
     e_cta += *cl.map_shared_rank(&sh.cta_eq, rr);
   }
+  uint32_t grun = 0u;  // the CTA's earlier groups' totals
 #pragma unroll
   for (int u = 0; u < NG; ++u) {
     if (u < ng) {
-      const uint32_t before = sh.gbase[u] + sh.wtot[u][warp];
+      const uint32_t before = grun + sh.wtot[u][warp];
+      grun += sh.gbase[u];
       uint32_t g = g_cta + (before >> 16) + ((ex_gt[u >> 2] >> (8 * (u & 3))) & 0xFFu);
       uint32_t e = e_cta + (before & 0xFFFFu) + ((ex_eq[u >> 2] >> (8 * (u & 3))) & 0xFFu);
       const uint4 kk = keys4[u * kThreads + tid];
