@@ -55,6 +55,7 @@ constexpr long long kWaitBudget = 2000000000LL;  // SM cycles (about 1 s)
 constexpr long long kTestWaitBudget = 2000000LL;  // SM cycles (about 1 ms): the test-only wait
 constexpr int kMaxRowsTc = 4096;                  // prefix table capacity
 constexpr int kMaxStages = 16;                    // key-tile ring depth at most
+constexpr int kTileCost0 = 4;                     // a tile's cost: kTileCost0 + its block's rows
 
 struct TcLayout {
   int hp;         // indexer heads padded to a multiple of 16
@@ -260,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t stage0 = base;
   const uint32_t q0 = base + lay.off_q;
   float *wbuf = reinterpret_cast<float *>(sb + lay.off_w);            // [NQ][NMAX]
-  int *prefix = reinterpret_cast<int *>(sb + lay.off_prefix);         // [R + 1]
+  int *prefix = reinterpret_cast<int *>(sb + lay.off_prefix);         // [R + 1] tiles before each block
+  int *cprefix = prefix + (p.max_rows + 1);                            // [R + 1] their cost before each block
   const uint32_t bar0 = base + lay.off_bar;
   // barrier map: full[S] empty[S] qfull[2] qempty[2] tfull[4] tempty[4] done
   auto FULL = [&](int s) { return bar0 + 8u * s; };
@@ -278,37 +280,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- tile counts per score block, prefix-summed (every CTA, redundantly)
   const int R = p.max_rows;
   for (int b = tid; b < R; b += kThreads) {
-    int nt = 0;
+    int nt = 0, cost = 0;
     const int nrows = p.block_nrows[b];
     if (nrows > 0) {
       const int first = p.block_first[b];
       bool ok = nrows <= p.block_rows && first >= 0 && first + nrows <= R;
       const int req = ok ? p.row_req[first] : 0;
       ok = ok && req >= 0 && req < p.max_reqs;
-      int lmax = 0;
+      int lmax = 0, nin = 0;
       for (int i = 0; i < nrows && ok; ++i) {  // checked over the whole block
         const int L = p.row_len[first + i];
         if (p.row_req[first + i] != req || L < 0 || L > p.score_width) ok = false;
-        if (first + i >= p.row_lo && first + i < p.row_hi) lmax = max(lmax, L);  // rows scored here
+        if (first + i >= p.row_lo && first + i < p.row_hi) {  // rows scored here
+          lmax = max(lmax, L);
+          ++nin;
+        }
       }
       if (!ok) {
         if (blockIdx.x == 0) flag_status(p.status, DSA_DEV_BAD_BLOCK);
       } else {
         nt = (lmax + kTok - 1) / kTok;  // 0 for a block outside the window
+        cost = nt * (kTileCost0 + nin);
       }
     }
     prefix[b + 1] = nt;
+    cprefix[b + 1] = cost;
   }
   if (tid == 0) {
     prefix[0] = 0;
+    cprefix[0] = 0;
     misc[1] = 0;
   }
   __syncthreads();
-  {
+  // inclusive scans of both (in place)
+  auto scan = [&](int *arr) {
     const int per = (R + kThreads - 1) / kThreads;
     const int lo = 1 + tid * per, hi = min(R + 1, lo + per);
     int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += prefix[i];
+    for (int i = lo; i < hi; ++i) sum += arr[i];
     int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -320,14 +329,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = incl - sum;
     for (int w2 = 0; w2 < warp; ++w2) run += misc[2 + w2];
     for (int i = lo; i < hi; ++i) {
-      run += prefix[i];
-      prefix[i] = run;
+      run += arr[i];
+      arr[i] = run;
     }
     __syncthreads();
-  }
+  };
+  scan(prefix);
+  scan(cprefix);
+  // The CTA's tiles: an equal share of the total cost.  A tile of a score
+  // block with n rows costs kTileCost0 + n units: a block's rows share its
+  // key tiles, but each row adds MMA columns and epilogue sums, so equal
+  // tile counts left the CTAs holding 4-row prefill blocks ~50% longer than
+  // those holding decode rows (per-CTA end times, mixed and 1M prefill
+  // steps; a 4-row tile at 1.6 decode tiles balanced both within a few
+  // percent).  Tile t of block b starts at cost cprefix[b] + t * w_b; the
+  // CTA takes the tiles whose start falls in its share, so the shares tile
+  // the row order without gaps or overlaps.  Decode-only steps (every block
+  // one row) keep equal tile counts.
   const int total = prefix[R];
-  const int beg = static_cast<int>((static_cast<long long>(blockIdx.x) * total) / gridDim.x);
-  const int end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total) / gridDim.x);
+  const int ctotal = cprefix[R];
+  auto tile_at = [&](int c) {  // the first tile whose cost start is >= c
+    if (c >= ctotal) return total;
+    const int b = find_block(cprefix, R, c);
+    const int nt = prefix[b + 1] - prefix[b];
+    const int w = (cprefix[b + 1] - cprefix[b]) / nt;
+    return prefix[b] + (c - cprefix[b] + w - 1) / w;
+  };
+  const int beg = tile_at(static_cast<int>((static_cast<long long>(blockIdx.x) * ctotal) / gridDim.x));
+  const int end = tile_at(static_cast<int>((static_cast<long long>(blockIdx.x + 1) * ctotal) / gridDim.x));
   if (beg >= end) return;  // uniform across the CTA
   BlockCache bc;
   bc.tab = reinterpret_cast<int *>(sb + lay.off_blk);
@@ -815,19 +844,20 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
   const int kSmemFloor = ctas_per_sm == 2 ? 80 * 1024 : 120 * 1024;
   const uint32_t stageB = kTok * RB * ATOMS;
   const uint32_t qbufB = static_cast<uint32_t>(lay.n_max) * RB * ATOMS * (F8 ? 2 : 1);
+  // everything but the stages and their two barriers each
   auto fixed = [&](int nq) {
     uint32_t off = nq * qbufB;                    // query buffers (after the stages)
     off += nq * lay.n_max * 4;                    // weights
-    off += (cfg.max_rows + 1) * 4 + 16;           // prefix table
+    off += 2 * (cfg.max_rows + 1) * 4 + 16;       // tile and cost prefix tables
     off += kBlkCache * 8 * 4;                     // block cache
-    off += (2 * kMaxStages + 13) * 8 + 64;        // barriers (upper bound) + misc
-    return off + 1024 + 34 * 4;                   // alignment slack, scan scratch
+    off += 13 * 8;                                // the other barriers
+    return off + 1024 + 34 * 4;                   // alignment slack, misc and scan scratch
   };
   lay.nq = 2;
-  int stages = static_cast<int>((kSmemLimit - fixed(2)) / stageB);
+  int stages = static_cast<int>((kSmemLimit - fixed(2)) / (stageB + 16));
   if (stages < 4) {
     lay.nq = 1;
-    stages = static_cast<int>((kSmemLimit - fixed(1)) / stageB);
+    stages = static_cast<int>((kSmemLimit - fixed(1)) / (stageB + 16));
   }
   stages = stages > kMaxStages ? kMaxStages : stages;
   if (stages < 2) return cudaErrorInvalidValue;
@@ -838,7 +868,7 @@ cudaError_t launch_tc(const dsa_config_t &cfg, const IndexerParams &p, cudaStrea
   lay.off_w = off;
   off += lay.nq * lay.n_max * 4;
   lay.off_prefix = off;
-  off += (cfg.max_rows + 1) * 4;
+  off += 2 * (cfg.max_rows + 1) * 4;
   off = (off + 15u) & ~15u;
   lay.off_blk = off;
   off += kBlkCache * 8 * 4;
