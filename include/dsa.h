@@ -396,8 +396,11 @@ dsa_status_t dsa_merge(const dsa_config_t *cfg, const float *part_m, const float
  * and the top-k run once per row window (dsa_score_windows) on one score
  * buffer of window_rows rows, each window's indexer starting after the
  * previous window's top-k has finished; the results equal those of one
- * window.  The top-k, attention and merge launch with programmatic
- * dependent launch, so each one's start overlaps its predecessor's tail.
+ * window.  Rows of length 0 (pad rows) get out = 0 and lse = -inf without
+ * split partials: the step writes none for them (dsa_sparse_attn called on
+ * its own writes empty ones, which dsa_merge reads).  The top-k, attention
+ * and merge launch with programmatic dependent launch, so each one's start
+ * overlaps its predecessor's tail.
  * The whole step is capturable into one CUDA graph: no host sync,
  * allocation or host read, static grids.
  */

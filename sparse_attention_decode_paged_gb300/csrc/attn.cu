@@ -436,6 +436,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxKvHeads), 2) sparse_attn_kernel(
     for (int k = 0; k < nmine; ++k) {
       const RowSplit x = item_split(p, item_tab, ncache, k, false);
       if (x.L < 0) continue;  // a prefill-group row: its partials come from the group kernel
+      if (x.L == 0 && p.skip_empty_rows) continue;  // a pad row inside dsa_step: nothing reads its partials
       // A operand: this group's query heads (rows 8..15 are zero padding)
       uint32_t qa[D / 16][2];
 #pragma unroll

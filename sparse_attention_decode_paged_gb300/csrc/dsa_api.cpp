@@ -458,11 +458,16 @@ dsa_status_t dsa_topk_window(const dsa_config_t *cfg, int32_t row_begin, int32_t
   return topk_impl(cfg, row_begin, row_end, scores, row_len, topk_idx, workspace, hist, stream);
 }
 
-dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void *k_cache,
-                             const void *v_cache, const int32_t *page_table,
-                             const int32_t *row_req, const int32_t *row_len,
-                             const int32_t *topk_idx, float *part_m, float *part_l,
-                             float *part_acc, void *workspace, dsa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// The attention calls; inside dsa_step (skip_empty_rows) the rows of length
+// 0 get no split partials, since the step's merge writes their outputs
+// without reading them.
+dsa_status_t attn_impl(const dsa_config_t *cfg, const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *page_table, const int32_t *row_req, const int32_t *row_len,
+                       const int32_t *topk_idx, float *part_m, float *part_l, float *part_acc, void *workspace,
+                       bool skip_empty_rows, dsa_stream_t stream) {
   DSA_CHECK_CFG(cfg);
   DSA_CHECK_DEV_PTR(q);
   DSA_CHECK_DEV_PTR(k_cache);
@@ -507,6 +512,7 @@ dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void 
   p.page_shift = 0;
   while ((1 << p.page_shift) < cfg->page_size) ++p.page_shift;  // page_size is a validated power of two
   p.grouped = nullptr;
+  p.skip_empty_rows = skip_empty_rows ? 1 : 0;
   if (dsa::group_path_enabled(*cfg)) {
     // prefill row groups: the union, the other rows (the decode kernel leaves
     // the grouped rows alone), then the groups' tensor-core attention, whose
@@ -520,6 +526,18 @@ dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void 
     return cuda_status(e, "prefill-group attention launch");
   }
   return cuda_status(dsa::launch_sparse_attn(*cfg, p, stream), "sparse attention launch");
+}
+}  // namespace
+
+extern "C" {
+
+dsa_status_t dsa_sparse_attn(const dsa_config_t *cfg, const void *q, const void *k_cache,
+                             const void *v_cache, const int32_t *page_table,
+                             const int32_t *row_req, const int32_t *row_len,
+                             const int32_t *topk_idx, float *part_m, float *part_l,
+                             float *part_acc, void *workspace, dsa_stream_t stream) {
+  return attn_impl(cfg, q, k_cache, v_cache, page_table, row_req, row_len, topk_idx, part_m, part_l, part_acc,
+                   workspace, false, stream);
 }
 
 
@@ -555,8 +573,8 @@ dsa_status_t dsa_step(const dsa_config_t *cfg, const dsa_step_args_t *a, void *w
     st = topk_impl(cfg, lo, hi, scores, a->row_len, topk_idx, workspace, true, stream);
     if (st != DSA_OK) return st;
   }
-  st = dsa_sparse_attn(cfg, a->q, a->k_cache, a->v_cache, a->page_table, a->row_req, a->row_len,
-                       topk_idx, part_m, part_l, part_acc, workspace, stream);
+  st = attn_impl(cfg, a->q, a->k_cache, a->v_cache, a->page_table, a->row_req, a->row_len, topk_idx, part_m,
+                 part_l, part_acc, workspace, true, stream);
   if (st != DSA_OK) return st;
   // the step knows its rows: pad rows are written empty without their partials
   return merge_impl(cfg, part_m, part_l, part_acc, a->out, a->lse, a->row_len, stream);

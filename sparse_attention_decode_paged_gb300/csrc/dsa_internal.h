@@ -55,6 +55,7 @@ struct AttnParams {
   int32_t kv_interleaved;  // 1: one copy moves a token's K and V rows
   int32_t page_shift;      // log2(page_size)
   const int32_t *grouped;  // [R] 1: the row is attended by the prefill-group kernel (null: no groups)
+  int32_t skip_empty_rows; // 1: rows of length 0 get no partials (the step's merge never reads them)
 };
 
 // Prefill row groups: the rows of one request in a slot of kGroupRows

@@ -215,6 +215,8 @@ def test_split_partials_vs_oracle(problem, dsa_lib):
     grouped = _grouped_rows(dev, dsa_lib)
     for r in sample:
         L = int(rows["row_len"][r])
+        if L == 0:  # dsa_step writes no partials for pad rows (the separate call does: see below)
+            continue
         sel = idx[r][idx[r] >= 0]
         if grouped[r]:
             m, l, acc = _group_row_partials(inp, rows, idx, grouped, q, r)
@@ -259,3 +261,8 @@ def test_step_equals_separate_calls_bitwise(problem, dsa_lib):
     assert torch.equal(v["topk_idx"], dev.views["topk_idx"])
     assert torch.equal(out.view(torch.int16), t["out"].view(torch.int16))
     assert torch.equal(lse, t["lse"])
+    # dsa_sparse_attn on its own writes empty partials for the pad rows
+    # (m = -inf, l = 0, acc = 0): its merge reads every row
+    n = dev.rows["num_rows"]
+    assert torch.isneginf(v["part_m"][n:]).all()
+    assert (v["part_l"][n:] == 0).all() and (v["part_acc"][n:] == 0).all()
