@@ -107,14 +107,16 @@ __device__ __forceinline__ void merge_one(const float *part_m, const float *part
   if (lse && lane == 0) lse[rh] = lsum > 0.f ? mx + logf(lsum) : -INFINITY;
 }
 
-// PPW (row, head) merges per warp when S <= kMergeRound / PPW: the warp's
-// PPW * S partial slices are contiguous (layout [R*Hq, S, D]) and all issued
-// in one round, so a small S does not leave the warp one short round trip.
-// Lane j * SMAX + s holds m and l of split s of the warp's pair j.
-template <int D, int PPW>
+// PPW (row, head) merges per warp when S <= SMAX: the warp's PPW * S
+// partial slices are contiguous (layout [R*Hq, S, D]) and all issued in one
+// round, so a small S does not leave the warp one short round trip.  Lane
+// j * SMAX + s holds m and l of split s of the warp's pair j.  SMAX is S
+// rounded up to the kernels built (the registers holding the slices, and
+// with them the warps an SM keeps, follow PPW * SMAX).
+template <int D, int PPW, int SMAX>
 __device__ __forceinline__ void merge_multi(const MergeParams &p, long long rh0, long long total, int lane) {
+  static_assert(PPW * SMAX <= 32, "one lane per (pair, split)");
   constexpr int VN = D / 32;
-  constexpr int SMAX = kMergeRound / PPW;
   using VecT = typename std::conditional<VN == 4, float4, float2>::type;
   const int S = p.num_splits;
   const int mj = lane / SMAX, msl = lane - mj * SMAX;  // this lane's (pair, split) for m and l
@@ -166,11 +168,14 @@ __device__ __forceinline__ void merge_multi(const MergeParams &p, long long rh0,
   }
 }
 
-// Merges per warp for S splits (a power of two, so the kernels stay few).
+// Merges per warp for S splits and the splits' lanes per pair (few kernels).
 inline int merge_pairs_per_warp(int S) { return S <= 3 ? 8 : S <= 6 ? 4 : S <= 12 ? 2 : 1; }
+inline int merge_split_lanes(int S) {
+  return S <= 3 ? S : S == 4 ? 4 : S <= 6 ? 6 : S <= 8 ? 8 : S <= 12 ? 12 : 32;
+}
 
-template <int D, int PPW>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+template <int D, int PPW, int SMAX>
+__global__ void __launch_bounds__(256, (PPW * SMAX * D <= 16 * 128 ? 3 : 2)) merge_kernel(const MergeParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long total = static_cast<long long>(p.max_rows) * p.num_q_heads;
   const long long rh0 = (static_cast<long long>(blockIdx.x) * 8 + warp) * PPW;  // first (row, head)
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   if constexpr (PPW == 1)
     merge_one<D>(p.part_m, p.part_l, p.part_acc, rh0, p.num_splits, p.out, p.lse, lane);
   else
-    merge_multi<D, PPW>(p, rh0, total, lane);
+    merge_multi<D, PPW, SMAX>(p, rh0, total, lane);
 }
 
 struct AttnLayout {
@@ -610,15 +615,26 @@ cudaError_t launch_sparse_attn(const dsa_config_t &cfg, const AttnParams &p, cud
 
 cudaError_t launch_merge(const dsa_config_t &cfg, const MergeParams &p, cudaStream_t st) {
   const long long pairs = static_cast<long long>(cfg.max_rows) * cfg.num_q_heads;
-  const int ppw = merge_pairs_per_warp(cfg.num_splits);
+  const int ppw = merge_pairs_per_warp(cfg.num_splits), sl = merge_split_lanes(cfg.num_splits);
   const unsigned blocks = static_cast<unsigned>((pairs + 8LL * ppw - 1) / (8LL * ppw));
   void (*k)(const MergeParams) = nullptr;
+  auto pick = [&](auto d) -> void (*)(const MergeParams) {
+    constexpr int D = decltype(d)::value;
+    switch (sl) {
+      case 1: return merge_kernel<D, 8, 1>;
+      case 2: return merge_kernel<D, 8, 2>;
+      case 3: return merge_kernel<D, 8, 3>;
+      case 4: return merge_kernel<D, 4, 4>;
+      case 6: return merge_kernel<D, 4, 6>;
+      case 8: return merge_kernel<D, 2, 8>;
+      case 12: return merge_kernel<D, 2, 12>;
+      default: return merge_kernel<D, 1, 32>;
+    }
+  };
   if (cfg.head_dim == 128)
-    k = ppw == 8 ? merge_kernel<128, 8> : ppw == 4 ? merge_kernel<128, 4> : ppw == 2 ? merge_kernel<128, 2>
-                                                                                      : merge_kernel<128, 1>;
+    k = pick(std::integral_constant<int, 128>());
   else if (cfg.head_dim == 64)
-    k = ppw == 8 ? merge_kernel<64, 8> : ppw == 4 ? merge_kernel<64, 4> : ppw == 2 ? merge_kernel<64, 2>
-                                                                                    : merge_kernel<64, 1>;
+    k = pick(std::integral_constant<int, 64>());
   else
     return cudaErrorInvalidValue;
   cudaError_t e = launch_pdl(k, dim3(blocks), dim3(256), 0, st, 1u, p);
