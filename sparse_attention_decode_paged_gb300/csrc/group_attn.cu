@@ -148,33 +148,48 @@ __global__ void __launch_bounds__(kUnionThreads) group_union_kernel(const AttnPa
     s_len[tid] = L;
     s_n[tid] = mem ? min(p.topk, L) : 0;
   }
+  const int32_t *pt = p.page_table + static_cast<size_t>(max(req, 0)) * p.max_pages_per_req;
+  // the page of this thread's first 16 positions (an input, not the top-k's
+  // output): fetched before the wait, so the first scan does not wait on it
+  constexpr int kPer = kUnionScan / kUnionThreads;
+  const int pg_first = members != 0u && tid * kPer < lmax ? pt[(tid * kPer) >> p.page_shift] : -1;
   pdl_wait();  // the selection comes from the top-k kernel
   __syncthreads();
-  const int32_t *pt = p.page_table + static_cast<size_t>(max(req, 0)) * p.max_pages_per_req;
   const int K = p.topk;
   int ntile = 0, total = 0;  // tiles holding a selected position, selected positions
   for (int c0 = 0; c0 < lmax && members != 0u; c0 += kUnionSpan) {
     for (int i = tid; i < kUnionSpan / 2; i += kUnionThreads) mask2[i] = 0u;
     __syncthreads();
-    // every member's entries at once (entry i of member j at j * K + i), so
-    // the loads of all members are in flight together
-#pragma unroll 8
-    for (int f = tid; f < kGroupRows * K; f += kUnionThreads) {
-      const int j = f / K, i = f - j * K;
-      if (i >= s_n[j]) continue;  // no member, or past its selected entries
-      const int t = p.topk_idx[static_cast<size_t>(slot * kGroupRows + j) * K + i];
-      if (t == -1) continue;
-      if (t < 0 || t >= s_len[j]) {
-        if (c0 == 0) flag_status(p.status, DSA_DEV_BAD_INDEX);
-        continue;
+    // every member's entries (entry i of member j at j * K + i), 16 per
+    // thread loaded before any is used, so the loads of all members are in
+    // flight together
+    for (int f0 = 0; f0 < kGroupRows * K; f0 += 16 * kUnionThreads) {
+      int tv[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int f = f0 + u * kUnionThreads + tid;
+        const int j = f / K, i = f - j * K;
+        tv[u] = f < kGroupRows * K && i < s_n[j]  // no member, or past its selected entries: none
+                    ? p.topk_idx[static_cast<size_t>(slot * kGroupRows + j) * K + i]
+                    : -1;
       }
-      if (t >= c0 && t < c0 + kUnionSpan) atomicOr(&mask2[(t - c0) >> 1], (1u << j) << (16 * ((t - c0) & 1)));
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int f = f0 + u * kUnionThreads + tid;
+        const int j = f / K, t = tv[u];
+        if (t == -1) continue;
+        if (t < 0 || t >= s_len[j]) {
+          if (c0 == 0) flag_status(p.status, DSA_DEV_BAD_INDEX);
+          continue;
+        }
+        if (t >= c0 && t < c0 + kUnionSpan) atomicOr(&mask2[(t - c0) >> 1], (1u << j) << (16 * ((t - c0) & 1)));
+      }
     }
     __syncthreads();
     for (int s0 = c0; s0 < min(c0 + kUnionSpan, lmax); s0 += kUnionScan) {
       // thread t: positions s0 + 16t .. +15 (8 threads per 128-position tile);
       // a selected position on a page outside the pool is flagged and left out
-      constexpr int per = kUnionScan / kUnionThreads;  // 16, all on one page (page_size >= 16)
+      constexpr int per = kPer;  // 16, all on one page (page_size >= 16)
       int cnt = 0;
       uint32_t m16[per];  // per position: its 16 row bits
       uint32_t any = 0u;
@@ -186,7 +201,7 @@ __global__ void __launch_bounds__(kUnionThreads) group_union_kernel(const AttnPa
         any |= w;
       }
       if (any != 0u) {
-        const int pg = pt[(s0 + tid * per) >> p.page_shift];
+        const int pg = s0 == 0 ? pg_first : pt[(s0 + tid * per) >> p.page_shift];
         const bool bad = pg < 0 || pg >= p.num_pages;
         if (bad) flag_status(p.status, DSA_DEV_BAD_PAGE);
 #pragma unroll
